@@ -1,5 +1,5 @@
 """Streamed run of a whole-model workload (config 4 or 5) at full size, checked
-against the oracle on sampled tensors and by exact properties on every tensor.
+against the oracle on every element of every tensor.
 
 Run as a script (a child process of the GPU test, so that its pinned host memory
 is returned when it exits):  python tests/big_config_check.py <config>
@@ -18,7 +18,6 @@ sys.path.insert(0, os.path.dirname(HERE))
 sys.path.insert(0, HERE)
 
 import numpy as np  # noqa: E402
-import torch  # noqa: E402
 
 import oracle  # noqa: E402
 from oracle.runner import run_config  # noqa: E402
@@ -30,12 +29,6 @@ from parity import check_tensor, oracle_dict, state_dict  # noqa: E402
 # Host bytes the run holds beyond the pinned states: the oracle's per-tensor copy,
 # the CPU grad bank while it is built, comparison copies, the CUDA/torch runtime.
 HEADROOM = 24 << 30
-
-
-def sample_units(cfg):
-    last = cfg.n_units - 1
-    mid = (cfg.n_units - 1) // 2
-    return sorted({0, 1, mid, last - 1, last})       # embed, first/middle/last layer, head
 
 
 def main(cid: int) -> int:
@@ -55,35 +48,31 @@ def main(cid: int) -> int:
     sr.pool.sync(1_800_000)
     t_run = time.time() - t0
 
-    # Oracle on every element of the sampled units' tensors, one tensor at a time.
+    # The oracle on every tensor, one at a time: its inputs regenerated from the
+    # tensor's seed (never read back from the GPU side), freed after the comparison.
+    t0 = time.time()
+    threads = os.cpu_count() or 1
     gs = inputs.GradSource(cfg)
-    orc = oracle.Oracle()
-    sample = [j for u in sample_units(cfg) for j in cfg.unit_tensors(u)]
-    bad = 0
-    for j in sample:
-        ref = run_config(cfg, tensors=[j], threads=os.cpu_count() or 1, grad_source=gs)[j]
+    orc = oracle.Oracle(threads=threads)
+    bad = checked = checked_params = 0
+    for j in range(len(cfg.tensors)):
+        ref = run_config(cfg, tensors=[j], threads=threads, grad_source=gs)[j]
         partial = np.zeros(ref.acc.size, np.float32)
         for k in range(cfg.accum_steps - 1):
             orc.accum(partial, inputs.as_u16(gs(j, cfg.steps - 1, k)))
         rep = check_tensor(state_dict(sr.state, j), dict(oracle_dict(ref), acc=partial),
                            f"config {cid} tensor {j}")
         bad += sum(rep.values())
-        del ref
-    # On every tensor: delta = fl(master - widen(orig)) and w = rne(master), exactly.
-    for j, t in enumerate(sr.state.tensors):
-        master = t["master"].numpy()
-        orig = (t["orig"].view(torch.int16).numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
-        delta = t["delta"].numpy()
-        assert np.array_equal((master - orig).view(np.uint32), delta.view(np.uint32)), j
-        w = t["w"].view(torch.int16).numpy().view(np.uint16)
-        assert np.array_equal(orc.f32_to_bf16(master), w), j
-        assert np.all(t["v"].numpy() >= 0), j
+        checked += 1
+        checked_params += cfg.tensors[j].numel
+        del ref, partial
+    t_check = time.time() - t0
     sr.close()
-    print(json.dumps({"config": cid, "params": cfg.params, "sampled_tensors": len(sample),
-                      "sampled_params": sum(cfg.tensors[j].numel for j in sample),
+    print(json.dumps({"config": cid, "params": cfg.params, "tensors": len(cfg.tensors),
+                      "tensors_checked": checked, "params_checked": checked_params,
                       "non_bit_exact": bad, "setup_s": round(t_setup, 1),
-                      "run_s": round(t_run, 1)}))
-    return 0 if bad == 0 else 1
+                      "run_s": round(t_run, 1), "check_s": round(t_check, 1)}))
+    return 0 if (bad == 0 and checked_params == cfg.params) else 1
 
 
 if __name__ == "__main__":

@@ -31,4 +31,5 @@ def test_whole_model_streamed_full_size(cid):
         pytest.skip(f"not enough host memory for config {cid}: {tail}")
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
     res = json.loads(tail)
+    assert res["tensors_checked"] == res["tensors"] and res["params_checked"] == res["params"]
     assert res["non_bit_exact"] == 0
