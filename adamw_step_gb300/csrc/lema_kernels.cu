@@ -198,9 +198,6 @@ __device__ __forceinline__ void accum_chunk(const AccDesc* __restrict__ dp, cons
     }
 }
 
-
-// merged = bf16(base + delta): one fp32 add, round to nearest even (8 B/element:
-
 template <int kSplit>
 __global__ void __launch_bounds__(kThreads)
 accum_grad_kernel(const AccDesc* __restrict__ descs, const Chunk* __restrict__ chunks) {
@@ -216,6 +213,7 @@ accum_grad_kernel_v(const __grid_constant__ DescTable<AccDesc, N> t,
     accum_chunk<kSplit>(&t.d[c.tensor], c);
 }
 
+// merged = bf16(base + delta): one fp32 add, round to nearest even (8 B/element:
 // read bf16 2 + fp32 4, write bf16 2).
 __global__ void __launch_bounds__(kThreads)
 merge_kernel(const MergeDesc* __restrict__ descs, const Chunk* __restrict__ chunks) {
