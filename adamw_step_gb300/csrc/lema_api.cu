@@ -491,22 +491,81 @@ int run_accum_q8(const AccDescQ8* descs, int32_t count, cudaStream_t stream) {
         "8-bit accumulate launch");
 }
 
-int run_step_q8(const StepDescQ8* descs, int32_t count, const StepScalars& s, cudaStream_t stream) {
+int run_step_q8(const StepDescQ8* descs, int32_t count, const StepScalars& s, cudaStream_t stream,
+                unsigned int* gave_up) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (count <= kValueTableMax)
         return launch_by_value(
             descs, count, stream, validate_step_q8(descs, count),
             [&](const StepDescQ8* d, const Chunk* c, int64_t n) {
-                return launch_step_q8_v(d, count, c, n, s, stream);
+                return launch_step_q8_v(d, count, c, n, s, gave_up, stream);
             },
             "8-bit adamw step launch");
     return stage_and_launch(
         descs, count, stream, validate_step_q8(descs, count),
         [&](const StepDescQ8* d, const Chunk* c, int64_t n) {
-            return launch_step_q8(d, c, n, s, stream);
+            return launch_step_q8(d, c, n, s, gave_up, stream);
         },
         "8-bit adamw step launch");
 }
+
+// ------------------------------------------------- kernel give-up reporting ----
+
+int gave_up_flag_alloc(GaveUpFlag* f) {
+    void* h = nullptr;
+    cudaError_t e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) return cuda_error(e, "cudaHostAlloc (kernel status word)");
+    std::memset(h, 0, 64);
+    void* d = nullptr;
+    e = cudaHostGetDevicePointer(&d, h, 0);
+    if (e != cudaSuccess) {
+        cudaFreeHost(h);
+        return cuda_error(e, "cudaHostGetDevicePointer (kernel status word)");
+    }
+    f->host = static_cast<volatile unsigned int*>(h);
+    f->dev = static_cast<unsigned int*>(d);
+    return LEMA_OK;
+}
+
+void gave_up_flag_free(GaveUpFlag* f) {
+    if (f->host) cudaFreeHost(const_cast<unsigned int*>(f->host));
+    f->host = nullptr;
+    f->dev = nullptr;
+}
+
+int gave_up_take(const GaveUpFlag& f, const char* where) {
+    if (!f.host || *f.host == 0u) return LEMA_OK;
+    *f.host = 0u;
+    return set_error(LEMA_ERR_TIMEOUT,
+                     "%s: an 8-bit step kernel gave up waiting for its staged inputs (see "
+                     "lema_kernel_wait_timeouts); the groups it had not finished kept their old "
+                     "outputs, so that step's results are incomplete",
+                     where);
+}
+
+namespace {
+
+// The flag of the direct 8-bit step calls, one per device (allocated on first use).
+int direct_flag(GaveUpFlag** out) {
+    constexpr int kMaxDevices = 64;
+    static GaveUpFlag flags[kMaxDevices];
+    static std::mutex mu;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return set_error(LEMA_ERR_STATE, "device %d is beyond the %d devices supported", dev,
+                         kMaxDevices);
+    std::lock_guard<std::mutex> g(mu);
+    if (!flags[dev].host) {
+        const int rc = gave_up_flag_alloc(&flags[dev]);
+        if (rc != LEMA_OK) return rc;
+    }
+    *out = &flags[dev];
+    return LEMA_OK;
+}
+
+}  // namespace
 
 }  // namespace lema
 
@@ -515,6 +574,12 @@ int run_step_q8(const StepDescQ8* descs, int32_t count, const StepScalars& s, cu
 using namespace lema;
 
 extern "C" const char* lema_last_error(void) { return g_err; }
+
+extern "C" int lema_test_kernel_wait_limit(int64_t limit_ns) {
+    g_err[0] = '\0';
+    const cudaError_t e = set_wait_limit(limit_ns);
+    return e == cudaSuccess ? LEMA_OK : cuda_error(e, "setting the kernel wait limit");
+}
 
 extern "C" int lema_kernel_wait_timeouts(int64_t* count) {
     g_err[0] = '\0';
@@ -703,7 +768,12 @@ extern "C" int lema_adamw_step_q8(const lema_tensor_q8* tensors, int32_t count, 
             if (p && !aligned16(p))
                 return set_error(LEMA_ERR_ALIGN, "tensor %d: base address not 16-byte aligned", j);
     }
-    return run_step_q8(d.data(), count, s, static_cast<cudaStream_t>(cuda_stream));
+    GaveUpFlag* flag = nullptr;
+    rc = direct_flag(&flag);
+    if (rc != LEMA_OK) return rc;
+    rc = gave_up_take(*flag, "lema_adamw_step_q8 (an earlier call; nothing was launched now)");
+    if (rc != LEMA_OK) return rc;
+    return run_step_q8(d.data(), count, s, static_cast<cudaStream_t>(cuda_stream), flag->dev);
 }
 
 extern "C" int lema_merge_delta(const lema_merge* items, int32_t count, void* cuda_stream) {

@@ -332,6 +332,17 @@ static_assert(kGroup == 8 * kQBlock, "a group is whole quantization blocks");
 // Kernel-side bounded waits that ran out (read by lema_kernel_wait_timeouts).
 __device__ unsigned long long g_wait_timeouts = 0;
 
+// How long a wait for a group's staged inputs may take before the CTA gives up.
+// The copies of one 22 KB group take microseconds, so the default of 1 s is only
+// reached when something is wrong.  A test hook may lower it (0: give up at the
+// first poll that finds the copies still in flight) to exercise the give-up path.
+constexpr uint64_t kWaitNs = 1000000000ull;
+__device__ unsigned long long g_wait_limit_ns = kWaitNs;
+// After a give-up, the CTA still waits for the copies it has issued before its
+// shared memory goes away; that drain has its own, longer bound, which the test
+// hook does not change.
+constexpr uint64_t kDrainNs = 10000000000ull;
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -350,8 +361,16 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait for the phase of parity `parity` of an mbarrier to complete, giving up after
-// about `limit_ns`.
+// about `limit_ns` (limit_ns == 0: one non-blocking test, no wait).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (limit_ns == 0) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        return done != 0;
+    }
     uint64_t start = 0;
     for (uint32_t i = 0;; ++i) {
         uint32_t done;
@@ -367,8 +386,6 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64
         }
     }
 }
-
-constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: copies of 22 KB take microseconds
 
 struct Group {
     const StepDescQ8* dp;
@@ -506,8 +523,13 @@ __device__ __forceinline__ void step_direct(const StepScalars& s, const Group& g
 // group from a buffer (whole groups) or with plain loads (the rest).  Buffer j has
 // one mbarrier; after a group every thread meets at a CTA barrier and thread 0
 // refills the buffer with the group Op::kBufs steps ahead.
+//
+// A wait that runs out stops the CTA: it counts the event in g_wait_timeouts, sets
+// *gave_up (a word in host-mapped memory the host library reads after the launch has
+// finished; may be null), waits (bounded by kDrainNs) for the copies it has issued,
+// and returns.  The groups it had not finished keep their old outputs.
 template <typename Op>
-__device__ __forceinline__ void ring_run(const Op& op, int64_t n_groups) {
+__device__ __forceinline__ void ring_run(const Op& op, int64_t n_groups, unsigned int* gave_up) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t bars[Op::kBufs];
     const int lane = threadIdx.x & 31;
@@ -527,12 +549,13 @@ __device__ __forceinline__ void ring_run(const Op& op, int64_t n_groups) {
     }
     __syncthreads();   // barriers initialized before anyone waits on them
 
+    const uint64_t limit_ns = *const_cast<const volatile unsigned long long*>(&g_wait_limit_ns);
     int64_t k = 0;
     for (int64_t w = blockIdx.x; w < n_groups; w += G, ++k) {
         const int j = int(k % Op::kBufs);
         const uint32_t parity = uint32_t((k / Op::kBufs) & 1);
         const auto g = op.group(w);
-        const bool ok = wait_phase(smem_addr(&bars[j]), parity, kWaitNs);
+        const bool ok = wait_phase(smem_addr(&bars[j]), parity, limit_ns);
         if (ok && !g.empty) {
             if (g.full) op.staged(g, ring + j * Op::kStageBytes, lane);
             else op.direct(g, lane);
@@ -543,11 +566,16 @@ __device__ __forceinline__ void ring_run(const Op& op, int64_t n_groups) {
             // the CTA's shared memory goes away, and stop.
             if (threadIdx.x == 0) {
                 atomicAdd(&g_wait_timeouts, 1ull);
+                if (gave_up) {
+                    *reinterpret_cast<volatile unsigned int*>(gave_up) = 1u;
+                    __threadfence_system();
+                }
+                // The groups issued and not yet consumed: k .. k + kBufs - 1.
                 for (int64_t q = 0; q < Op::kBufs; ++q) {
                     const int64_t kq = k + q;
                     if (blockIdx.x + kq * G >= n_groups) break;
                     wait_phase(smem_addr(&bars[kq % Op::kBufs]), uint32_t((kq / Op::kBufs) & 1),
-                               kWaitNs);
+                               kDrainNs);
                 }
             }
             return;
@@ -583,8 +611,8 @@ struct StepOp {
 template <bool kPow2>
 __global__ void __launch_bounds__(kThreads, kStepCtasPerSm)
 adamw_q8_kernel(const StepDescQ8* __restrict__ descs, const Chunk* __restrict__ chunks,
-                int64_t n_groups, const StepScalars s) {
-    ring_run(StepOp<kPow2>{descs, chunks, s}, n_groups);
+                int64_t n_groups, const StepScalars s, unsigned int* gave_up) {
+    ring_run(StepOp<kPow2>{descs, chunks, s}, n_groups, gave_up);
 }
 
 __device__ __forceinline__ void accum_q8_chunk(const AccDescQ8* __restrict__ dp, const Chunk c) {
@@ -691,8 +719,8 @@ accum_q8_kernel_v(const __grid_constant__ DescTable<AccDescQ8, N> t, const Chunk
 template <bool kPow2, int N>
 __global__ void __launch_bounds__(kThreads, kStepCtasPerSm)
 adamw_q8_kernel_v(const __grid_constant__ DescTable<StepDescQ8, N> t, const Chunk* __restrict__ chunks,
-                  int64_t n_groups, const StepScalars s) {
-    ring_run(StepOp<kPow2>{&t.d[0], chunks, s}, n_groups);
+                  int64_t n_groups, const StepScalars s, unsigned int* gave_up) {
+    ring_run(StepOp<kPow2>{&t.d[0], chunks, s}, n_groups, gave_up);
 }
 
 }  // namespace
@@ -751,7 +779,7 @@ cudaError_t launch_accum_q8(const AccDescQ8* descs, const Chunk* chunks, int64_t
 }
 
 cudaError_t launch_step_q8(const StepDescQ8* descs, const Chunk* chunks, int64_t n_chunks,
-                           const StepScalars& s, cudaStream_t stream) {
+                           const StepScalars& s, unsigned int* gave_up, cudaStream_t stream) {
     if (n_chunks <= 0) return cudaSuccess;
     int n_sm = 0;
     const cudaError_t e = ring_setup(&n_sm);
@@ -759,9 +787,11 @@ cudaError_t launch_step_q8(const StepDescQ8* descs, const Chunk* chunks, int64_t
     const int64_t n_groups = n_chunks * kGroupsPerChunk;
     const unsigned grid = unsigned(std::min<int64_t>(n_groups, int64_t(n_sm) * kStepCtasPerSm));
     if (s.accum_pow2)
-        adamw_q8_kernel<true><<<grid, kThreads, kStepSmem, stream>>>(descs, chunks, n_groups, s);
+        adamw_q8_kernel<true><<<grid, kThreads, kStepSmem, stream>>>(descs, chunks, n_groups, s,
+                                                                     gave_up);
     else
-        adamw_q8_kernel<false><<<grid, kThreads, kStepSmem, stream>>>(descs, chunks, n_groups, s);
+        adamw_q8_kernel<false><<<grid, kThreads, kStepSmem, stream>>>(descs, chunks, n_groups, s,
+                                                                      gave_up);
     return cudaGetLastError();
 }
 
@@ -780,7 +810,8 @@ cudaError_t launch_accum_q8_v(const AccDescQ8* host_descs, int32_t count, const 
 }
 
 cudaError_t launch_step_q8_v(const StepDescQ8* host_descs, int32_t count, const Chunk* chunks,
-                             int64_t n_chunks, const StepScalars& s, cudaStream_t stream) {
+                             int64_t n_chunks, const StepScalars& s, unsigned int* gave_up,
+                             cudaStream_t stream) {
     if (n_chunks <= 0) return cudaSuccess;
     if (count > kValueTableMax) return cudaErrorInvalidValue;
     int n_sm = 0;
@@ -791,21 +822,26 @@ cudaError_t launch_step_q8_v(const StepDescQ8* host_descs, int32_t count, const 
     if (count <= kValueTableSmall) {
         const auto t = table_of<StepDescQ8, kValueTableSmall>(host_descs, count);
         if (s.accum_pow2)
-            adamw_q8_kernel_v<true, kValueTableSmall><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s);
+            adamw_q8_kernel_v<true, kValueTableSmall><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s, gave_up);
         else
-            adamw_q8_kernel_v<false, kValueTableSmall><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s);
+            adamw_q8_kernel_v<false, kValueTableSmall><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s, gave_up);
     } else {
         const auto t = table_of<StepDescQ8, kValueTableMax>(host_descs, count);
         if (s.accum_pow2)
-            adamw_q8_kernel_v<true, kValueTableMax><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s);
+            adamw_q8_kernel_v<true, kValueTableMax><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s, gave_up);
         else
-            adamw_q8_kernel_v<false, kValueTableMax><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s);
+            adamw_q8_kernel_v<false, kValueTableMax><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s, gave_up);
     }
     return cudaGetLastError();
 }
 
 cudaError_t read_wait_timeouts(unsigned long long* out) {
     return cudaMemcpyFromSymbol(out, g_wait_timeouts, sizeof(*out));
+}
+
+cudaError_t set_wait_limit(int64_t ns) {
+    const unsigned long long v = ns < 0 ? kWaitNs : static_cast<unsigned long long>(ns);
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof v);
 }
 
 }  // namespace lema

@@ -17,11 +17,19 @@
 // so the next unit's host-to-device copy into a slot's input half never races the
 // device-to-host copy out of its output half.
 //
-// Ordering (per slot s, per unit L):
-//   H2D(L)  waits step_done[s] (input half free) and the D2H events that last wrote
-//           the host buffers it reads; records in_ready[s].
-//   step(L) waits in_ready[s] and out_drained[s] (output half free); records step_done[s].
-//   D2H(L)  waits step_done[s]; records out_drained[s] and unit_done[L].
+// A unit laid out packed (LEMA_UNIT_PACKED) is moved in up to kMaxSlices slices of
+// whole chunks: slice q's host-to-device copies, its kernel and its device-to-host
+// copies each start as soon as slice q of the stage before is done, so the first
+// kernel starts after one slice has arrived instead of the whole unit, and the
+// last unit's results start leaving before its last slice is computed.
+//
+// Ordering (per slot s, per unit L, per slice q):
+//   H2D(L, q)  (from q = 0: waits step_done[s], the input half free, and the D2H
+//              events that last wrote the host buffers it reads); records in_ready[s][q].
+//   step(L, q) (from q = 0: waits out_drained[s], the output half free); waits
+//              in_ready[s][q]; records done[s][q]; after the last slice step_done[s].
+//   D2H(L, q)  waits done[s][q]; after the last slice records out_drained[s] and
+//              unit_done[L].
 // Every wait is a device-side stream wait; the host never blocks inside a call.
 #include <algorithm>
 #include <atomic>
@@ -39,6 +47,9 @@ using namespace lema;
 
 namespace {
 
+constexpr int kMaxSlices = 8;             // slices of one unit (see lema_pool_slices)
+constexpr int64_t kSliceAlign = kChunk;    // slice boundaries: whole chunks
+
 struct Slot {
     float* master = nullptr;
     float* m = nullptr;
@@ -51,7 +62,8 @@ struct Slot {
     float* v_o = nullptr;
     float* delta = nullptr;
     uint16_t* w = nullptr;
-    cudaEvent_t in_ready = nullptr, step_done = nullptr, out_drained = nullptr;
+    cudaEvent_t in_ready[kMaxSlices] = {}, done[kMaxSlices] = {};
+    cudaEvent_t step_done = nullptr, out_drained = nullptr;
 };
 
 constexpr int64_t kTensorAlign = 64;  // elements; keeps every sub-array 128-byte aligned
@@ -112,6 +124,10 @@ struct lema_pool {
     std::unordered_map<const void*, size_t> last_writer;  // host buffer -> unit_done index
     std::unordered_map<const void*, int> kinds;            // memory_kind() of checked pointers
     int64_t next_slot = 0;
+    GaveUpFlag gave_up;   // set by an 8-bit step kernel of this pool whose wait ran out
+    bool copies_only = false;   // measurement mode: no kernels (lema_pool_copies_only)
+    int32_t max_slices = 4;                   // lema_pool_slices
+    int64_t min_slice = int64_t(8) << 20;     // elements
     std::mutex mu;
     // Stage tracing (off unless lema_pool_trace enabled it): a timed event pair per
     // stage of each unit, recorded on the stage's stream after its waits.
@@ -160,7 +176,10 @@ void destroy_pool(lema_pool* p) {
     if (p->d2h) cudaStreamSynchronize(p->d2h);
     clear_trace(p);
     for (Slot& s : p->slots) {
-        if (s.in_ready) cudaEventDestroy(s.in_ready);
+        for (int q = 0; q < kMaxSlices; ++q) {
+            if (s.in_ready[q]) cudaEventDestroy(s.in_ready[q]);
+            if (s.done[q]) cudaEventDestroy(s.done[q]);
+        }
         if (s.step_done) cudaEventDestroy(s.step_done);
         if (s.out_drained) cudaEventDestroy(s.out_drained);
     }
@@ -172,12 +191,29 @@ void destroy_pool(lema_pool* p) {
     if (p->cmp) cudaStreamDestroy(p->cmp);
     if (p->d2h) cudaStreamDestroy(p->d2h);
     if (p->slab) cudaFree(p->slab);
+    gave_up_flag_free(&p->gave_up);
     delete p;
 }
 
 int new_event(cudaEvent_t* e) {
     cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
     return r == cudaSuccess ? LEMA_OK : cuda_error(r, "cudaEventCreate");
+}
+
+// The slices of a unit whose packed span holds n_span elements: S pieces, bound[0]
+// = 0 < bound[1] < ... < bound[S] = n_span, inner boundaries on whole chunks, each
+// piece at least the pool's minimum slice; S = 1 for a unit that is not packed.
+int unit_slices(const lema_pool* p, bool packed, int64_t n_span, int64_t* bound) {
+    bound[0] = 0;
+    int64_t want = packed ? std::min<int64_t>(p->max_slices, n_span / p->min_slice) : 1;
+    want = std::max<int64_t>(1, std::min<int64_t>(want, kMaxSlices));
+    int S = 0;
+    for (int64_t q = 1; q < want; ++q) {
+        const int64_t b = round_up(n_span * q / want, kSliceAlign);
+        if (b > bound[S] && b < n_span) bound[++S] = b;
+    }
+    bound[++S] = n_span;
+    return S;
 }
 
 // memory_kind() once per pointer per pool: the driver's lookup grows with the number
@@ -325,14 +361,22 @@ extern "C" int lema_pool_create(int32_t n_slots, int64_t slot_params, lema_pool*
         auto b16 = [&](uint16_t*& dst) { dst = reinterpret_cast<uint16_t*>(b); b += 2 * P; };
         f32(s.master); f32(s.m); f32(s.v); f32(s.acc); b16(s.orig); b16(s.grad);
         f32(s.master_o); f32(s.m_o); f32(s.v_o); f32(s.delta); b16(s.w);
-        int rc;
-        if ((rc = new_event(&s.in_ready)) || (rc = new_event(&s.step_done)) ||
-            (rc = new_event(&s.out_drained))) {
+        int rc = new_event(&s.step_done);
+        if (rc == LEMA_OK) rc = new_event(&s.out_drained);
+        for (int q = 0; q < kMaxSlices && rc == LEMA_OK; ++q) {
+            rc = new_event(&s.in_ready[q]);
+            if (rc == LEMA_OK) rc = new_event(&s.done[q]);
+        }
+        if (rc != LEMA_OK) {
             destroy_pool(p);
             return rc;
         }
     }
     int rc;
+    if ((rc = gave_up_flag_alloc(&p->gave_up)) != LEMA_OK) {
+        destroy_pool(p);
+        return rc;
+    }
     if ((rc = new_event(&p->entry)) || (rc = new_event(&p->tail[0])) ||
         (rc = new_event(&p->tail[1])) || (rc = new_event(&p->tail[2]))) {
         destroy_pool(p);
@@ -367,7 +411,7 @@ extern "C" int lema_pool_sync(lema_pool* pool, int32_t timeout_ms) {
             if (e == cudaErrorNotReady) { pending = true; continue; }
             if (e != cudaSuccess) return cuda_error(e, "pool work failed");
         }
-        if (!pending) return LEMA_OK;
+        if (!pending) return gave_up_take(pool->gave_up, "lema_pool_sync");
         if (std::chrono::steady_clock::now() >= deadline)
             return set_error(LEMA_ERR_TIMEOUT, "pool work still pending after %d ms", timeout_ms);
         std::this_thread::sleep_for(std::chrono::microseconds(50));
@@ -378,6 +422,28 @@ extern "C" int lema_pool_wait_stream(lema_pool* pool, void* cuda_stream) {
     clear_error();
     if (!pool) return set_error(LEMA_ERR_ARG, "pool is NULL");
     for (cudaEvent_t ev : pool->tail) LEMA_TRY(wait_on(static_cast<cudaStream_t>(cuda_stream), ev));
+    return LEMA_OK;
+}
+
+extern "C" int lema_pool_slices(lema_pool* pool, int32_t max_slices, int64_t min_slice_params) {
+    clear_error();
+    if (!pool) return set_error(LEMA_ERR_ARG, "pool is NULL");
+    if (max_slices < 1 || max_slices > kMaxSlices)
+        return set_error(LEMA_ERR_ARG, "max_slices must lie in [1, %d] (got %d)", kMaxSlices,
+                         max_slices);
+    if (min_slice_params < 1) return set_error(LEMA_ERR_ARG, "min_slice_params must be >= 1");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    pool->max_slices = max_slices;
+    pool->min_slice = round_up(min_slice_params, kSliceAlign);
+    return LEMA_OK;
+}
+
+extern "C" int lema_pool_copies_only(lema_pool* pool, int32_t on) {
+    clear_error();
+    if (!pool) return set_error(LEMA_ERR_ARG, "pool is NULL");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    LEMA_TRY(lema_pool_sync(pool, 600000));
+    pool->copies_only = on != 0;
     return LEMA_OK;
 }
 
@@ -450,6 +516,8 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
     LEMA_TRY(begin_call(pool, n_layers, caller));
 
     const bool acc_in = micro_step >= 2;
+    const auto H2D = cudaMemcpyHostToDevice;
+    const auto D2H = cudaMemcpyDeviceToHost;
     std::vector<int64_t> off;
     std::vector<AccDesc> ad;
     std::vector<StepDesc> sd;
@@ -461,9 +529,38 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
         off.assign(size_t(ly.count), 0);
         for (int32_t j = 1; j < ly.count; ++j)
             off[size_t(j)] = off[size_t(j - 1)] + round_up(ly.tensors[j - 1].n, kTensorAlign);
+        // A packed unit moves each field in one copy per slice spanning its non-empty
+        // tensors (from the first one's pointer); otherwise one copy per tensor.
+        const bool packed = (ly.flags & LEMA_UNIT_PACKED) != 0;
+        int32_t first = -1, last = -1;
+        for (int32_t j = 0; j < ly.count; ++j)
+            if (ly.tensors[j].n > 0) {
+                if (first < 0) first = j;
+                last = j;
+            }
+        const int64_t base = first < 0 ? 0 : off[size_t(first)];
+        const int64_t n_span = first < 0 ? 0 : off[size_t(last)] + ly.tensors[last].n - base;
+        int64_t bound[kMaxSlices + 1];
+        const int S = unit_slices(pool, packed, n_span, bound);
+        // The part of tensor j in slice q, as [lo, hi) within the tensor (all of it
+        // when the unit is not sliced).
+        auto part = [&](int32_t j, int q, int64_t* lo, int64_t* hi) {
+            const int64_t n = ly.tensors[j].n, o = off[size_t(j)] - base;
+            if (S == 1) { *lo = 0; *hi = n; return; }
+            *lo = std::max<int64_t>(0, bound[q] - o);
+            *hi = std::min<int64_t>(n, bound[q + 1] - o);
+        };
+        // the fields' copies of slice q: (slot offset, host element offset, count)
+        auto field_copy = [&](int32_t j, int q, int64_t* o, int64_t* h, int64_t* n) {
+            if (!packed) { *o = off[size_t(j)]; *h = 0; *n = ly.tensors[j].n; return; }
+            if (j != first) { *n = 0; return; }
+            *o = base + bound[q];
+            *h = bound[q];
+            *n = bound[q + 1] - bound[q];
+        };
 
         // -- host -> device: the unit's inputs into the slot's input half (once a
-        // lower tier, if any, has put them into the host buffers).
+        // lower tier, if any, has put them into the host buffers), slice by slice.
         if (hooks) LEMA_TRY(hooks->before_unit(L));
         LEMA_TRY(wait_on(pool->h2d, sl.step_done));
         waits.clear();
@@ -474,115 +571,121 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
             for (const void* p : reads) note_writer(pool, p, waits);
         }
         LEMA_TRY(wait_for_writers(pool, waits));
-        int tr = -1;
-        LEMA_TRY(trace_open(pool, pool->h2d, LEMA_STAGE_H2D, L, &tr));
-        // A packed unit moves each field in one copy spanning its non-empty tensors
-        // (n_span elements from the first one's pointer); otherwise one per tensor.
-        const bool packed = (ly.flags & LEMA_UNIT_PACKED) != 0;
-        int32_t first = -1, last = -1;
-        for (int32_t j = 0; j < ly.count; ++j)
-            if (ly.tensors[j].n > 0) {
-                if (first < 0) first = j;
-                last = j;
-            }
-        const int64_t n_span =
-            first < 0 ? 0 : off[size_t(last)] + ly.tensors[last].n - off[size_t(first)];
-        for (int32_t j = 0; j < ly.count; ++j) {
-            const lema_tensor& t = ly.tensors[j];
-            const int64_t o = off[size_t(j)];
-            const int64_t n = packed ? (j == first ? n_span : 0) : t.n;
-            if (grad_on_host[size_t(L)][size_t(j)] && t.n > 0)
-                LEMA_TRY(copy_async(sl.grad + o, ly.grads[j], 2 * t.n, cudaMemcpyHostToDevice,
-                                    pool->h2d));
-            if (n == 0) continue;
-            if (acc_in) LEMA_TRY(copy_async(sl.acc + o, t.acc, 4 * n, cudaMemcpyHostToDevice, pool->h2d));
-            if (final_step) {
-                LEMA_TRY(copy_async(sl.master + o, t.master, 4 * n, cudaMemcpyHostToDevice, pool->h2d));
-                LEMA_TRY(copy_async(sl.m + o, t.m, 4 * n, cudaMemcpyHostToDevice, pool->h2d));
-                LEMA_TRY(copy_async(sl.v + o, t.v, 4 * n, cudaMemcpyHostToDevice, pool->h2d));
-                LEMA_TRY(copy_async(sl.orig + o, t.orig_bf16, 2 * n, cudaMemcpyHostToDevice, pool->h2d));
-            }
-        }
-        LEMA_TRY(trace_close(pool, pool->h2d, tr));
-        LEMA_TRY(record(sl.in_ready, pool->h2d));
-
-        // -- compute, from the input half into the output half: accumulate-only
-        // micro-steps add the grad into a new partial sum; the last micro-step folds
-        // its grad into the out-of-place AdamW step (one launch, acc not written).
-        LEMA_TRY(wait_on(pool->cmp, sl.in_ready));
-        LEMA_TRY(wait_on(pool->cmp, sl.out_drained));
-        LEMA_TRY(trace_open(pool, pool->cmp, LEMA_STAGE_COMPUTE, L, &tr));
-        if (!final_step) {
-            ad.clear();
+        for (int q = 0; q < S; ++q) {
+            int tr = -1;
+            LEMA_TRY(trace_open(pool, pool->h2d, LEMA_STAGE_H2D, L, &tr));
             for (int32_t j = 0; j < ly.count; ++j) {
-                const int64_t o = off[size_t(j)];
-                AccDesc a;
-                a.acc_in = acc_in ? sl.acc + o : nullptr;
-                a.acc_out = sl.delta + o;
-                a.grad = grad_on_host[size_t(L)][size_t(j)] ? sl.grad + o : ly.grads[j];
-                a.n = ly.tensors[j].n;
-                ad.push_back(a);
-            }
-            LEMA_TRY(run_accum(ad.data(), ly.count, pool->cmp));
-        } else {
-            sd.clear();
-            for (int32_t j = 0; j < ly.count; ++j) {
-                const int64_t o = off[size_t(j)];
-                StepDesc x;
-                x.master_in = sl.master + o;
-                x.m_in = sl.m + o;
-                x.v_in = sl.v + o;
-                x.acc = acc_in ? sl.acc + o : nullptr;
-                x.orig = sl.orig + o;
-                x.master_out = sl.master_o + o;
-                x.m_out = sl.m_o + o;
-                x.v_out = sl.v_o + o;
-                x.delta = sl.delta + o;
-                x.w = sl.w + o;
-                x.grad = grad_on_host[size_t(L)][size_t(j)] ? sl.grad + o : ly.grads[j];
-                x.n = ly.tensors[j].n;
-                x.flags = 0;
-                sd.push_back(x);
-            }
-            LEMA_TRY(run_step(sd.data(), ly.count, s, pool->cmp));
-        }
-        LEMA_TRY(trace_close(pool, pool->cmp, tr));
-        LEMA_TRY(record(sl.step_done, pool->cmp));
-
-        // -- device -> host: results out of the slot's output half.
-        LEMA_TRY(wait_on(pool->d2h, sl.step_done));
-        LEMA_TRY(trace_open(pool, pool->d2h, LEMA_STAGE_D2H, L, &tr));
-        for (int32_t j = 0; j < ly.count; ++j) {
-            const lema_tensor& t = ly.tensors[j];
-            const int64_t o = off[size_t(j)];
-            const int64_t n = packed ? (j == first ? n_span : 0) : t.n;
-            float* mo = t.master_out ? t.master_out : t.master;
-            float* m_o = t.m_out ? t.m_out : t.m;
-            float* v_o = t.v_out ? t.v_out : t.v;
-            // every tensor's own host buffers name this unit as their writer (a packed
-            // unit moves them in the first tensor's span copy), so a later call that
-            // groups the tensors differently still waits for these copies
-            if (t.n > 0) {
-                if (!final_step) {
-                    pool->last_writer[t.acc] = size_t(L);
-                } else {
-                    pool->last_writer[mo] = size_t(L);
-                    pool->last_writer[m_o] = size_t(L);
-                    pool->last_writer[v_o] = size_t(L);
+                const lema_tensor& t = ly.tensors[j];
+                int64_t lo = 0, hi = 0;
+                part(j, q, &lo, &hi);
+                if (grad_on_host[size_t(L)][size_t(j)] && hi > lo)
+                    LEMA_TRY(copy_async(sl.grad + off[size_t(j)] + lo, ly.grads[j] + lo,
+                                        2 * (hi - lo), H2D, pool->h2d));
+                int64_t o = 0, h = 0, n = 0;
+                field_copy(j, q, &o, &h, &n);
+                if (n == 0) continue;
+                if (acc_in) LEMA_TRY(copy_async(sl.acc + o, t.acc + h, 4 * n, H2D, pool->h2d));
+                if (final_step) {
+                    LEMA_TRY(copy_async(sl.master + o, t.master + h, 4 * n, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.m + o, t.m + h, 4 * n, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.v + o, t.v + h, 4 * n, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.orig + o, t.orig_bf16 + h, 2 * n, H2D, pool->h2d));
                 }
             }
-            if (n == 0) continue;
+            LEMA_TRY(trace_close(pool, pool->h2d, tr));
+            LEMA_TRY(record(sl.in_ready[q], pool->h2d));
+        }
+
+        // -- compute, from the input half into the output half, slice by slice:
+        // accumulate-only micro-steps add the grad into a new partial sum; the last
+        // micro-step folds its grad into the out-of-place AdamW step (acc not written).
+        LEMA_TRY(wait_on(pool->cmp, sl.out_drained));
+        for (int q = 0; q < S; ++q) {
+            LEMA_TRY(wait_on(pool->cmp, sl.in_ready[q]));
+            int tr = -1;
+            LEMA_TRY(trace_open(pool, pool->cmp, LEMA_STAGE_COMPUTE, L, &tr));
+            ad.clear();
+            sd.clear();
+            for (int32_t j = 0; j < ly.count; ++j) {
+                int64_t lo = 0, hi = 0;
+                part(j, q, &lo, &hi);
+                if (S > 1 && hi <= lo) continue;
+                const int64_t o = off[size_t(j)] + lo;
+                const uint16_t* g = grad_on_host[size_t(L)][size_t(j)] ? sl.grad + o
+                                                                        : ly.grads[j] + lo;
+                if (!final_step) {
+                    AccDesc a;
+                    a.acc_in = acc_in ? sl.acc + o : nullptr;
+                    a.acc_out = sl.delta + o;
+                    a.grad = g;
+                    a.n = hi - lo;
+                    ad.push_back(a);
+                } else {
+                    StepDesc x;
+                    x.master_in = sl.master + o;
+                    x.m_in = sl.m + o;
+                    x.v_in = sl.v + o;
+                    x.acc = acc_in ? sl.acc + o : nullptr;
+                    x.orig = sl.orig + o;
+                    x.master_out = sl.master_o + o;
+                    x.m_out = sl.m_o + o;
+                    x.v_out = sl.v_o + o;
+                    x.delta = sl.delta + o;
+                    x.w = sl.w + o;
+                    x.grad = g;
+                    x.n = hi - lo;
+                    x.flags = 0;
+                    sd.push_back(x);
+                }
+            }
+            if (!pool->copies_only) {
+                if (!final_step) LEMA_TRY(run_accum(ad.data(), int32_t(ad.size()), pool->cmp));
+                else LEMA_TRY(run_step(sd.data(), int32_t(sd.size()), s, pool->cmp));
+            }
+            LEMA_TRY(trace_close(pool, pool->cmp, tr));
+            LEMA_TRY(record(sl.done[q], pool->cmp));
+        }
+        LEMA_TRY(record(sl.step_done, pool->cmp));
+
+        // -- device -> host: results out of the slot's output half, slice by slice.
+        // Every tensor's own host buffers name this unit as their writer (a packed
+        // unit moves them in the first tensor's span copies), so a later call that
+        // groups the tensors differently still waits for these copies.
+        for (int32_t j = 0; j < ly.count; ++j) {
+            const lema_tensor& t = ly.tensors[j];
+            if (t.n == 0) continue;
             if (!final_step) {
-                LEMA_TRY(copy_async(t.acc, sl.delta + o, 4 * n, cudaMemcpyDeviceToHost, pool->d2h));
+                pool->last_writer[t.acc] = size_t(L);
             } else {
-                LEMA_TRY(copy_async(mo, sl.master_o + o, 4 * n, cudaMemcpyDeviceToHost, pool->d2h));
-                LEMA_TRY(copy_async(m_o, sl.m_o + o, 4 * n, cudaMemcpyDeviceToHost, pool->d2h));
-                LEMA_TRY(copy_async(v_o, sl.v_o + o, 4 * n, cudaMemcpyDeviceToHost, pool->d2h));
-                LEMA_TRY(copy_async(t.delta, sl.delta + o, 4 * n, cudaMemcpyDeviceToHost, pool->d2h));
-                LEMA_TRY(copy_async(t.w_bf16, sl.w + o, 2 * n, cudaMemcpyDeviceToHost, pool->d2h));
+                pool->last_writer[t.master_out ? t.master_out : t.master] = size_t(L);
+                pool->last_writer[t.m_out ? t.m_out : t.m] = size_t(L);
+                pool->last_writer[t.v_out ? t.v_out : t.v] = size_t(L);
             }
         }
-        LEMA_TRY(trace_close(pool, pool->d2h, tr));
+        for (int q = 0; q < S; ++q) {
+            LEMA_TRY(wait_on(pool->d2h, sl.done[q]));
+            int tr = -1;
+            LEMA_TRY(trace_open(pool, pool->d2h, LEMA_STAGE_D2H, L, &tr));
+            for (int32_t j = 0; j < ly.count; ++j) {
+                const lema_tensor& t = ly.tensors[j];
+                int64_t o = 0, h = 0, n = 0;
+                field_copy(j, q, &o, &h, &n);
+                if (n == 0) continue;
+                float* mo = t.master_out ? t.master_out : t.master;
+                float* m_o = t.m_out ? t.m_out : t.m;
+                float* v_o = t.v_out ? t.v_out : t.v;
+                if (!final_step) {
+                    LEMA_TRY(copy_async(t.acc + h, sl.delta + o, 4 * n, D2H, pool->d2h));
+                } else {
+                    LEMA_TRY(copy_async(mo + h, sl.master_o + o, 4 * n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(m_o + h, sl.m_o + o, 4 * n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(v_o + h, sl.v_o + o, 4 * n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(t.delta + h, sl.delta + o, 4 * n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(t.w_bf16 + h, sl.w + o, 2 * n, D2H, pool->d2h));
+                }
+            }
+            LEMA_TRY(trace_close(pool, pool->d2h, tr));
+        }
         LEMA_TRY(record(sl.out_drained, pool->d2h));
         LEMA_TRY(record(pool->unit_done[size_t(L)], pool->d2h));
         if (hooks) LEMA_TRY(hooks->after_unit(L, pool->d2h));
@@ -892,6 +995,9 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
                                  cudaStream_t caller, UnitHooks* hooks) {
     if (carved_q8_bytes(pool->slot_params) > pool->slot_params * 38)
         return set_error(LEMA_ERR_STATE, "slot too small for the 8-bit layout");
+    // A give-up in an earlier call that nobody has synced on yet: report it first.
+    LEMA_TRY(gave_up_take(pool->gave_up, "8-bit streamed call (an earlier call of this pool; "
+                                         "nothing was enqueued now)"));
     const bool final_step = micro_step == K;
     const bool acc_in = micro_step >= 2;
     std::vector<std::vector<char>> grad_on_host(static_cast<size_t>(n_layers));
@@ -907,6 +1013,7 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
     std::vector<size_t> waits;
     const auto H2D = cudaMemcpyHostToDevice;
     const auto D2H = cudaMemcpyDeviceToHost;
+    auto blocks = [](int64_t n) { return (n + kQBlock - 1) / kQBlock; };
     for (int32_t L = 0; L < n_layers; ++L) {
         const lema_layer_q8& ly = layers[L];
         Slot& sl0 = pool->slots[size_t(pool->next_slot % pool->n_slots)];
@@ -922,18 +1029,35 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
                 if (first < 0) first = j;
                 last = j;
             }
-        // a copy of tensor j moves n elements (and nb scales); a packed unit moves
-        // each field in one span from its first non-empty tensor
-        auto span = [&](int32_t j, int64_t* n, int64_t* nb) {
+        // The packed span starts at the first non-empty tensor (a multiple of 1024
+        // elements), so every slice boundary (whole chunks) is a whole number of
+        // blocks and each slice's scales start on a 16-byte boundary.
+        const int64_t base = first < 0 ? 0 : off[size_t(first)];
+        const int64_t n_span = first < 0 ? 0 : off[size_t(last)] + ly.tensors[last].n - base;
+        int64_t bound[kMaxSlices + 1];
+        const int S = unit_slices(pool, packed, n_span, bound);
+        auto part = [&](int32_t j, int q, int64_t* lo, int64_t* hi) {
+            const int64_t n = ly.tensors[j].n, o = off[size_t(j)] - base;
+            if (S == 1) { *lo = 0; *hi = n; return; }
+            *lo = std::max<int64_t>(0, bound[q] - o);
+            *hi = std::min<int64_t>(n, bound[q + 1] - o);
+        };
+        // slice q's copies of tensor j: slot offset o, host element offset h, n
+        // elements and nb scales (a packed unit: one span from its first tensor)
+        auto field_copy = [&](int32_t j, int q, int64_t* o, int64_t* h, int64_t* n,
+                              int64_t* nb) {
             if (!packed) {
+                *o = off[size_t(j)];
+                *h = 0;
                 *n = ly.tensors[j].n;
-                *nb = (*n + kQBlock - 1) / kQBlock;
+                *nb = blocks(*n);
                 return;
             }
             if (j != first) { *n = *nb = 0; return; }
-            *n = off[size_t(last)] + ly.tensors[last].n - off[size_t(first)];
-            *nb = (off[size_t(last)] - off[size_t(first)]) / kQBlock +
-                  (ly.tensors[last].n + kQBlock - 1) / kQBlock;
+            *o = base + bound[q];
+            *h = bound[q];
+            *n = bound[q + 1] - bound[q];
+            *nb = blocks(bound[q + 1]) - bound[q] / kQBlock;
         };
 
         // -- host -> device (once a lower tier, if any, has filled the host buffers)
@@ -947,117 +1071,139 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
             for (const void* p : reads) note_writer(pool, p, waits);
         }
         LEMA_TRY(wait_for_writers(pool, waits));
-        int tr = -1;
-        LEMA_TRY(trace_open(pool, pool->h2d, LEMA_STAGE_H2D, L, &tr));
-        for (int32_t j = 0; j < ly.count; ++j) {
-            const lema_tensor_q8& t = ly.tensors[j];
-            const int64_t o = off[size_t(j)], b = o / kQBlock;
-            if (grad_on_host[size_t(L)][size_t(j)] && t.n > 0)
-                LEMA_TRY(copy_async(sl.grad + o, ly.grads[j], 2 * t.n, H2D, pool->h2d));
-            int64_t n = 0, nb = 0;
-            span(j, &n, &nb);
-            if (n == 0) continue;
-            if (acc_in) {
-                LEMA_TRY(copy_async(sl.acc_q + o, t.acc_q, n, H2D, pool->h2d));
-                LEMA_TRY(copy_async(sl.acc_s + b, t.acc_scale, 4 * nb, H2D, pool->h2d));
-            }
-            if (final_step) {
-                LEMA_TRY(copy_async(sl.master + o, t.master, 4 * n, H2D, pool->h2d));
-                LEMA_TRY(copy_async(sl.m_q + o, t.m_q, n, H2D, pool->h2d));
-                LEMA_TRY(copy_async(sl.m_s + b, t.m_scale, 4 * nb, H2D, pool->h2d));
-                LEMA_TRY(copy_async(sl.r_q + o, t.r_q, n, H2D, pool->h2d));
-                LEMA_TRY(copy_async(sl.r_s + b, t.r_scale, 4 * nb, H2D, pool->h2d));
-                LEMA_TRY(copy_async(sl.orig + o, t.orig_bf16, 2 * n, H2D, pool->h2d));
-            }
-        }
-        LEMA_TRY(trace_close(pool, pool->h2d, tr));
-        LEMA_TRY(record(sl0.in_ready, pool->h2d));
-
-        // -- compute
-        LEMA_TRY(wait_on(pool->cmp, sl0.in_ready));
-        LEMA_TRY(wait_on(pool->cmp, sl0.out_drained));
-        LEMA_TRY(trace_open(pool, pool->cmp, LEMA_STAGE_COMPUTE, L, &tr));
-        if (!final_step) {
-            ad.clear();
+        for (int q = 0; q < S; ++q) {
+            int tr = -1;
+            LEMA_TRY(trace_open(pool, pool->h2d, LEMA_STAGE_H2D, L, &tr));
             for (int32_t j = 0; j < ly.count; ++j) {
-                const int64_t o = off[size_t(j)], b = o / kQBlock;
-                AccDescQ8 a;
-                a.acc_q_in = acc_in ? sl.acc_q + o : nullptr;
-                a.acc_scale_in = acc_in ? sl.acc_s + b : nullptr;
-                a.acc_q_out = sl.acc_q_o + o;
-                a.acc_scale_out = sl.acc_s_o + b;
-                a.grad = grad_on_host[size_t(L)][size_t(j)] ? sl.grad + o : ly.grads[j];
-                a.n = ly.tensors[j].n;
-                ad.push_back(a);
-            }
-            LEMA_TRY(run_accum_q8(ad.data(), ly.count, pool->cmp));
-        } else {
-            sd.clear();
-            for (int32_t j = 0; j < ly.count; ++j) {
-                const int64_t o = off[size_t(j)], b = o / kQBlock;
-                StepDescQ8 x;
-                x.master_in = sl.master + o;
-                x.m_q_in = sl.m_q + o;
-                x.m_scale_in = sl.m_s + b;
-                x.r_q_in = sl.r_q + o;
-                x.r_scale_in = sl.r_s + b;
-                x.acc_q = acc_in ? sl.acc_q + o : nullptr;
-                x.acc_scale = acc_in ? sl.acc_s + b : nullptr;
-                x.grad = grad_on_host[size_t(L)][size_t(j)] ? sl.grad + o : ly.grads[j];
-                x.orig = sl.orig + o;
-                x.master_out = sl.master_o + o;
-                x.m_q_out = sl.m_q_o + o;
-                x.m_scale_out = sl.m_s_o + b;
-                x.r_q_out = sl.r_q_o + o;
-                x.r_scale_out = sl.r_s_o + b;
-                x.delta = sl.delta + o;
-                x.w = sl.w + o;
-                x.n = ly.tensors[j].n;
-                x.flags = 0;
-                sd.push_back(x);
-            }
-            LEMA_TRY(run_step_q8(sd.data(), ly.count, s, pool->cmp));
-        }
-        LEMA_TRY(trace_close(pool, pool->cmp, tr));
-        LEMA_TRY(record(sl0.step_done, pool->cmp));
-
-        // -- device -> host
-        LEMA_TRY(wait_on(pool->d2h, sl0.step_done));
-        LEMA_TRY(trace_open(pool, pool->d2h, LEMA_STAGE_D2H, L, &tr));
-        for (int32_t j = 0; j < ly.count; ++j) {
-            const lema_tensor_q8& t = ly.tensors[j];
-            const int64_t o = off[size_t(j)], b = o / kQBlock;
-            int64_t n = 0, nb = 0;
-            span(j, &n, &nb);
-            float* mo = t.master_out ? t.master_out : t.master;
-            int8_t* mq = t.m_q_out ? t.m_q_out : t.m_q;
-            float* ms = t.m_scale_out ? t.m_scale_out : t.m_scale;
-            uint8_t* rq = t.r_q_out ? t.r_q_out : t.r_q;
-            float* rs = t.r_scale_out ? t.r_scale_out : t.r_scale;
-            if (t.n > 0) {          // as in lema_stream_layers: every tensor's buffers
-                if (!final_step) {
-                    pool->last_writer[t.acc_q] = size_t(L);
-                } else {
-                    pool->last_writer[mo] = size_t(L);
-                    pool->last_writer[mq] = size_t(L);
-                    pool->last_writer[rq] = size_t(L);
+                const lema_tensor_q8& t = ly.tensors[j];
+                int64_t lo = 0, hi = 0;
+                part(j, q, &lo, &hi);
+                if (grad_on_host[size_t(L)][size_t(j)] && hi > lo)
+                    LEMA_TRY(copy_async(sl.grad + off[size_t(j)] + lo, ly.grads[j] + lo,
+                                        2 * (hi - lo), H2D, pool->h2d));
+                int64_t o = 0, h = 0, n = 0, nb = 0;
+                field_copy(j, q, &o, &h, &n, &nb);
+                if (n == 0) continue;
+                const int64_t b = o / kQBlock, hb = h / kQBlock;
+                if (acc_in) {
+                    LEMA_TRY(copy_async(sl.acc_q + o, t.acc_q + h, n, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.acc_s + b, t.acc_scale + hb, 4 * nb, H2D, pool->h2d));
+                }
+                if (final_step) {
+                    LEMA_TRY(copy_async(sl.master + o, t.master + h, 4 * n, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.m_q + o, t.m_q + h, n, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.m_s + b, t.m_scale + hb, 4 * nb, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.r_q + o, t.r_q + h, n, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.r_s + b, t.r_scale + hb, 4 * nb, H2D, pool->h2d));
+                    LEMA_TRY(copy_async(sl.orig + o, t.orig_bf16 + h, 2 * n, H2D, pool->h2d));
                 }
             }
-            if (n == 0) continue;
+            LEMA_TRY(trace_close(pool, pool->h2d, tr));
+            LEMA_TRY(record(sl0.in_ready[q], pool->h2d));
+        }
+
+        // -- compute, slice by slice
+        LEMA_TRY(wait_on(pool->cmp, sl0.out_drained));
+        for (int q = 0; q < S; ++q) {
+            LEMA_TRY(wait_on(pool->cmp, sl0.in_ready[q]));
+            int tr = -1;
+            LEMA_TRY(trace_open(pool, pool->cmp, LEMA_STAGE_COMPUTE, L, &tr));
+            ad.clear();
+            sd.clear();
+            for (int32_t j = 0; j < ly.count; ++j) {
+                int64_t lo = 0, hi = 0;
+                part(j, q, &lo, &hi);
+                if (S > 1 && hi <= lo) continue;
+                const int64_t o = off[size_t(j)] + lo, b = o / kQBlock;
+                const uint16_t* g = grad_on_host[size_t(L)][size_t(j)] ? sl.grad + o
+                                                                        : ly.grads[j] + lo;
+                if (!final_step) {
+                    AccDescQ8 a;
+                    a.acc_q_in = acc_in ? sl.acc_q + o : nullptr;
+                    a.acc_scale_in = acc_in ? sl.acc_s + b : nullptr;
+                    a.acc_q_out = sl.acc_q_o + o;
+                    a.acc_scale_out = sl.acc_s_o + b;
+                    a.grad = g;
+                    a.n = hi - lo;
+                    ad.push_back(a);
+                } else {
+                    StepDescQ8 x;
+                    x.master_in = sl.master + o;
+                    x.m_q_in = sl.m_q + o;
+                    x.m_scale_in = sl.m_s + b;
+                    x.r_q_in = sl.r_q + o;
+                    x.r_scale_in = sl.r_s + b;
+                    x.acc_q = acc_in ? sl.acc_q + o : nullptr;
+                    x.acc_scale = acc_in ? sl.acc_s + b : nullptr;
+                    x.grad = g;
+                    x.orig = sl.orig + o;
+                    x.master_out = sl.master_o + o;
+                    x.m_q_out = sl.m_q_o + o;
+                    x.m_scale_out = sl.m_s_o + b;
+                    x.r_q_out = sl.r_q_o + o;
+                    x.r_scale_out = sl.r_s_o + b;
+                    x.delta = sl.delta + o;
+                    x.w = sl.w + o;
+                    x.n = hi - lo;
+                    x.flags = 0;
+                    sd.push_back(x);
+                }
+            }
+            if (!pool->copies_only) {
+                if (!final_step)
+                    LEMA_TRY(run_accum_q8(ad.data(), int32_t(ad.size()), pool->cmp));
+                else
+                    LEMA_TRY(run_step_q8(sd.data(), int32_t(sd.size()), s, pool->cmp,
+                                         pool->gave_up.dev));
+            }
+            LEMA_TRY(trace_close(pool, pool->cmp, tr));
+            LEMA_TRY(record(sl0.done[q], pool->cmp));
+        }
+        LEMA_TRY(record(sl0.step_done, pool->cmp));
+
+        // -- device -> host, slice by slice (every tensor's own buffers name this unit
+        // as their writer, as in lema_stream_layers)
+        for (int32_t j = 0; j < ly.count; ++j) {
+            const lema_tensor_q8& t = ly.tensors[j];
+            if (t.n == 0) continue;
             if (!final_step) {
-                LEMA_TRY(copy_async(t.acc_q, sl.acc_q_o + o, n, D2H, pool->d2h));
-                LEMA_TRY(copy_async(t.acc_scale, sl.acc_s_o + b, 4 * nb, D2H, pool->d2h));
+                pool->last_writer[t.acc_q] = size_t(L);
             } else {
-                LEMA_TRY(copy_async(mo, sl.master_o + o, 4 * n, D2H, pool->d2h));
-                LEMA_TRY(copy_async(mq, sl.m_q_o + o, n, D2H, pool->d2h));
-                LEMA_TRY(copy_async(ms, sl.m_s_o + b, 4 * nb, D2H, pool->d2h));
-                LEMA_TRY(copy_async(rq, sl.r_q_o + o, n, D2H, pool->d2h));
-                LEMA_TRY(copy_async(rs, sl.r_s_o + b, 4 * nb, D2H, pool->d2h));
-                LEMA_TRY(copy_async(t.delta, sl.delta + o, 4 * n, D2H, pool->d2h));
-                LEMA_TRY(copy_async(t.w_bf16, sl.w + o, 2 * n, D2H, pool->d2h));
+                pool->last_writer[t.master_out ? t.master_out : t.master] = size_t(L);
+                pool->last_writer[t.m_q_out ? t.m_q_out : t.m_q] = size_t(L);
+                pool->last_writer[t.r_q_out ? t.r_q_out : t.r_q] = size_t(L);
             }
         }
-        LEMA_TRY(trace_close(pool, pool->d2h, tr));
+        for (int q = 0; q < S; ++q) {
+            LEMA_TRY(wait_on(pool->d2h, sl0.done[q]));
+            int tr = -1;
+            LEMA_TRY(trace_open(pool, pool->d2h, LEMA_STAGE_D2H, L, &tr));
+            for (int32_t j = 0; j < ly.count; ++j) {
+                const lema_tensor_q8& t = ly.tensors[j];
+                int64_t o = 0, h = 0, n = 0, nb = 0;
+                field_copy(j, q, &o, &h, &n, &nb);
+                if (n == 0) continue;
+                const int64_t b = o / kQBlock, hb = h / kQBlock;
+                float* mo = t.master_out ? t.master_out : t.master;
+                int8_t* mq = t.m_q_out ? t.m_q_out : t.m_q;
+                float* ms = t.m_scale_out ? t.m_scale_out : t.m_scale;
+                uint8_t* rq = t.r_q_out ? t.r_q_out : t.r_q;
+                float* rs = t.r_scale_out ? t.r_scale_out : t.r_scale;
+                if (!final_step) {
+                    LEMA_TRY(copy_async(t.acc_q + h, sl.acc_q_o + o, n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(t.acc_scale + hb, sl.acc_s_o + b, 4 * nb, D2H, pool->d2h));
+                } else {
+                    LEMA_TRY(copy_async(mo + h, sl.master_o + o, 4 * n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(mq + h, sl.m_q_o + o, n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(ms + hb, sl.m_s_o + b, 4 * nb, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(rq + h, sl.r_q_o + o, n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(rs + hb, sl.r_s_o + b, 4 * nb, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(t.delta + h, sl.delta + o, 4 * n, D2H, pool->d2h));
+                    LEMA_TRY(copy_async(t.w_bf16 + h, sl.w + o, 2 * n, D2H, pool->d2h));
+                }
+            }
+            LEMA_TRY(trace_close(pool, pool->d2h, tr));
+        }
         LEMA_TRY(record(sl0.out_drained, pool->d2h));
         LEMA_TRY(record(pool->unit_done[size_t(L)], pool->d2h));
         if (hooks) LEMA_TRY(hooks->after_unit(L, pool->d2h));

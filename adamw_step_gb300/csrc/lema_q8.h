@@ -51,21 +51,39 @@ static_assert(sizeof(AccDescQ8) == 48, "AccDescQ8 layout");
 // Kernel launchers (lema_kernels_q8.cu).  `descs` and `chunks` are device tables.
 cudaError_t launch_accum_q8(const AccDescQ8* descs, const Chunk* chunks, int64_t n_chunks,
                             cudaStream_t stream);
+// gave_up: device-visible address of a word in host-mapped memory that the kernel
+// sets to 1 when one of its bounded waits runs out (may be null).
 cudaError_t launch_step_q8(const StepDescQ8* descs, const Chunk* chunks, int64_t n_chunks,
-                           const StepScalars& s, cudaStream_t stream);
+                           const StepScalars& s, unsigned int* gave_up, cudaStream_t stream);
 
 // By-value descriptor tables (at most kValueTableMax tensors), as launch_step_v.
 cudaError_t launch_accum_q8_v(const AccDescQ8* host_descs, int32_t count, const Chunk* chunks,
                               int64_t n_chunks, cudaStream_t stream);
 cudaError_t launch_step_q8_v(const StepDescQ8* host_descs, int32_t count, const Chunk* chunks,
-                             int64_t n_chunks, const StepScalars& s, cudaStream_t stream);
+                             int64_t n_chunks, const StepScalars& s, unsigned int* gave_up,
+                             cudaStream_t stream);
 
 // Count of kernel-side bounded waits (the staged 8-bit step's mbarrier waits) that
 // ran out since the library was loaded on this device.
 cudaError_t read_wait_timeouts(unsigned long long* out);
+// The staged 8-bit step's wait limit on the current device (ns < 0: the default).
+cudaError_t set_wait_limit(int64_t ns);
+
+// A word of host-mapped, page-locked memory that an 8-bit step kernel sets when a
+// bounded wait runs out: `host` is read by the library after the work has finished,
+// `dev` is the address passed to the kernel.
+struct GaveUpFlag {
+    volatile unsigned int* host = nullptr;
+    unsigned int* dev = nullptr;
+};
+int gave_up_flag_alloc(GaveUpFlag* f);
+void gave_up_flag_free(GaveUpFlag* f);
+// LEMA_ERR_TIMEOUT (and the flag cleared) when the flag is set, else LEMA_OK.
+int gave_up_take(const GaveUpFlag& f, const char* where);
 
 // Validate + build-or-reuse the device table + launch (lema_api.cu).
 int run_accum_q8(const AccDescQ8* descs, int32_t count, cudaStream_t stream);
-int run_step_q8(const StepDescQ8* descs, int32_t count, const StepScalars& s, cudaStream_t stream);
+int run_step_q8(const StepDescQ8* descs, int32_t count, const StepScalars& s, cudaStream_t stream,
+                unsigned int* gave_up);
 
 }  // namespace lema

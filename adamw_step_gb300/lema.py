@@ -154,10 +154,13 @@ def raw():
     lib.lema_status_string.argtypes = [ctypes.c_int]
     lib.lema_status_string.restype = ctypes.c_char_p
     lib.lema_pool_trace.argtypes = [c_void_p, c_int32]
+    lib.lema_pool_copies_only.argtypes = [c_void_p, c_int32]
+    lib.lema_pool_slices.argtypes = [c_void_p, c_int32, c_int64]
     lib.lema_pool_trace_read.argtypes = [c_void_p, ctypes.POINTER(LemaTraceEvent), c_int32,
                                          ctypes.POINTER(c_int32)]
     lib.lema_test_fail_copy.argtypes = [c_int64]
     lib.lema_test_fail_copy.restype = None
+    lib.lema_test_kernel_wait_limit.argtypes = [c_int64]
     for name in ("lema_accum_grad", "lema_adamw_step", "lema_adamw_step_noalloc",
                  "lema_accum_grad_q8", "lema_adamw_step_q8", "lema_merge_delta",
                  "lema_pool_create", "lema_stream_layers", "lema_stream_layers_q8",
@@ -165,7 +168,8 @@ def raw():
                  "lema_disk_sync", "lema_disk_close", "lema_stream_layers_disk",
                  "lema_stream_layers_disk_q8", "lema_disk_probe", "lema_kernel_wait_timeouts",
                  "lema_pool_sync", "lema_pool_wait_stream", "lema_pool_destroy",
-                 "lema_pool_trace", "lema_pool_trace_read"):
+                 "lema_pool_trace", "lema_pool_trace_read", "lema_test_kernel_wait_limit",
+                 "lema_pool_copies_only", "lema_pool_slices"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -274,6 +278,17 @@ def lema_pool_destroy(pool) -> None:
     _check(raw().lema_pool_destroy(pool))
 
 
+def lema_pool_slices(pool, max_slices: int, min_slice_params: int) -> None:
+    """Split packed units into at most max_slices slices of whole chunks, each at
+    least min_slice_params elements, so their copies and kernels overlap."""
+    _check(raw().lema_pool_slices(pool, int(max_slices), int(min_slice_params)))
+
+
+def lema_pool_copies_only(pool, on: bool) -> None:
+    """Measurement mode: streamed calls enqueue their copies but launch no kernel."""
+    _check(raw().lema_pool_copies_only(pool, 1 if on else 0))
+
+
 def lema_pool_trace(pool, max_events: int) -> None:
     _check(raw().lema_pool_trace(pool, int(max_events)))
 
@@ -287,7 +302,15 @@ def lema_pool_trace_read(pool, max_events: int = 1 << 16) -> list:
 
 
 def lema_test_fail_copy(nth_copy: int) -> None:
+    """Test hook: make the nth host<->device copy the pool enqueues fail (0 disarms)."""
     raw().lema_test_fail_copy(int(nth_copy))
+
+
+def lema_test_kernel_wait_limit(limit_ns: int) -> None:
+    """Test hook: the 8-bit step kernel's wait limit for its staged inputs on the
+    current device (< 0: the default; 0: give up at the first poll that finds the
+    copies in flight)."""
+    _check(raw().lema_test_kernel_wait_limit(int(limit_ns)))
 
 
 def lema_disk_layout(unit_params, q8: bool = False):

@@ -76,6 +76,12 @@ def parse():
                    help="time lema_merge_delta (bf16(base + delta)) on the workload's tensors")
     p.add_argument("--trace-out", default="",
                    help="streamed legs: record the pool's stage trace and write it (JSON) here")
+    p.add_argument("--no-hidden", action="store_true",
+                   help="streamed legs: skip the copies-only steps that show whether the "
+                        "compute is hidden behind the copies")
+    p.add_argument("--no-whole-model", action="store_true",
+                   help="default run: skip the whole-model streamed leg (TinyLlama-1.1B "
+                        "shape, states in pinned host RAM)")
     return p.parse_args()
 
 
@@ -329,7 +335,7 @@ def reference_arm(args, cfg, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": config_block(cfg, args, world),
+            "config": config_block(cfg, args, world, l2="CPU oracle (no GPU L2 involved)"),
             "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
                              "cores": min(threads, orc.max_threads()),
                              "sample": f"each step: one optimizer step (K={cfg.accum_steps} "
@@ -338,14 +344,34 @@ def reference_arm(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_block(cfg, args, world):
+L2_BYTES = 129e6   # GB300 L2
+
+
+def l2_label(bytes_per_launch) -> str:
+    """Whether the timed launches stream through L2 or may be served from it (no
+    flush runs between launches): from the smallest and largest bytes one launch
+    moves, against the 129 MB L2."""
+    lo, hi = min(bytes_per_launch) / 1e6, max(bytes_per_launch) / 1e6
+    span = f"{lo:.0f} MB" if abs(hi - lo) < 0.5 else f"{lo:.0f}-{hi:.0f} MB"
+    if lo > L2_BYTES / 1e6:
+        return f"inputs larger than L2: every launch moves {span} against a 129 MB L2, no flush"
+    if hi <= L2_BYTES / 1e6:
+        return (f"every launch moves {span}, within the 129 MB L2: partly L2-served (no flush "
+                "between launches), so its fractions are not DRAM-bound figures")
+    return (f"launches move {span} against a 129 MB L2: those below it are partly L2-served "
+            "(no flush between launches), the others stream through")
+
+
+def config_block(cfg, args, world, l2=None):
     n = len(cfg.tensors) if not args.tensors else args.tensors
-    return {"workload": cfg.name + (f" [first {n} tensors]" if args.tensors else "") +
-                        (" [8-bit moments and accumulators]" if getattr(args, "q8", False) else ""),
-            "params": sum(t.numel for t in cfg.tensors[:n]), "tensors": n,
-            "accum_steps": cfg.accum_steps, "residency": "hbm",
-            "parallelism": f"replicas x{world}",
-            "l2": "inputs larger than L2 (each launch streams > 129 MB), no flush"}
+    out = {"workload": cfg.name + (f" [first {n} tensors]" if args.tensors else "") +
+                       (" [8-bit moments and accumulators]" if getattr(args, "q8", False) else ""),
+           "params": sum(t.numel for t in cfg.tensors[:n]), "tensors": n,
+           "accum_steps": cfg.accum_steps, "residency": "hbm",
+           "parallelism": f"replicas x{world}"}
+    if l2 is not None:
+        out["l2"] = l2
+    return out
 
 
 # ----------------------------------------------------------------- streamed leg
@@ -383,6 +409,8 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
         write_trace(trace_out, cfg, sr, lema.lema_pool_trace_read(sr.pool.handle, 1 << 20))
     barrier(world)
     el = reduce_max(marks[0][0].elapsed_time(marks[-1][1]) / 1e3, world)
+    hidden = None if getattr(args, "no_hidden", False) else \
+        copies_only_steps(sr, stream, world, steps, warmup, el / steps)
     h2d, d2h = sr.link_bytes_per_step(host_grads=host_grads)
     floor = link_time_floor(h2d, d2h, peaks)
     per_step = el / steps
@@ -401,6 +429,7 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
            # host RAM of this process backed by transparent huge pages once the
            # states were allocated (the rest uses base pages)
            "host_state_bytes": sr.state.pinned.nbytes, "anon_huge_page_bytes": huge,
+           "compute_hidden": hidden,
            "path": f"lema_stream_layers{'_q8' if q8 else ''}, {cfg.n_slots} VRAM slots, "
                    f"3 streams, {'8-bit' if q8 else 'fp32'} states "
                    f"{'and bf16 grads ' if host_grads else ''}in pinned host RAM"}
@@ -408,6 +437,42 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
     del sr
     torch.cuda.empty_cache()
     return out
+
+
+def copies_only_steps(sr, stream, world, steps, warmup, real_s_per_step):
+    """The same streamed steps with the pool in its measurement mode (every copy,
+    event and stream wait enqueued, no kernel launched): how much the kernels add to
+    a streamed step.  hidden_ratio = real step time / copies-only step time; 1.0
+    means the compute is entirely hidden behind the host-link copies.  Leaves the
+    host states holding slot contents, not results: run after the real steps."""
+    import torch
+    from adamw_step_gb300 import lema
+    lema.lema_pool_copies_only(sr.pool.handle, True)
+    try:
+        for t in range(warmup):
+            sr.step(t, stream)
+        sr.wait(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        marks = [(ev(), ev()) for _ in range(steps)]
+        for i in range(steps):
+            marks[i][0].record(stream)
+            sr.step(warmup + i, stream)
+            sr.wait(stream)
+            marks[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    finally:
+        lema.lema_pool_copies_only(sr.pool.handle, False)
+    el = reduce_max(marks[0][0].elapsed_time(marks[-1][1]) / 1e3, world)
+    each = sorted(a.elapsed_time(b) for a, b in marks)
+    med = each[len(each) // 2]
+    return {"copies_only_ms_per_step": 1e3 * el / steps, "copies_only_ms_median": med,
+            "copies_only_ms_each_step": [round(a.elapsed_time(b), 2) for a, b in marks],
+            "hidden_ratio": real_s_per_step / (el / steps),
+            "how": "the same steps with lema_pool_copies_only on: all copies and stream "
+                   "ordering, no kernels; ratio = real / copies-only time per step"}
 
 
 VALUE_TABLE_MAX = 64   # calls of at most this many tensors pass their table by value
@@ -568,7 +633,8 @@ def streamed_main(cfg, args, rank, world):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": leg["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "data": "synthetic",
-                "config": dict(config_block(cfg, args, world),
+                "config": dict(config_block(cfg, args, world, l2="bound by the disk; "
+                                            "no L2 reuse across units"),
                                residency="disk file + pinned-RAM accumulators, streamed"),
                 "roofline": roof, "disk": leg, "clocks": clk, "cpu_baseline": None,
                 "gpu_launches": args.steps * sum(
@@ -602,7 +668,9 @@ def streamed_main(cfg, args, rank, world):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": leg["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "data": "synthetic",
-                "config": dict(config_block(cfg, args, world), residency="pinned host, streamed"),
+                "config": dict(config_block(cfg, args, world, l2="bound by the host link; "
+                                            "no L2 reuse across units"),
+                               residency="pinned host, streamed"),
                 "roofline": roof, "streamed": leg, "clocks": clk, "cpu_baseline": cpu,
                 "gpu_launches": args.steps * sum(
                     cfg.accum_steps * launches_per_call(len(cfg.unit_tensors(u)), args.q8)
@@ -644,7 +712,8 @@ def merge_main(cfg, args, rank, world):
                           "unit": UNIT, "n_gpus": world, "steps": args.steps,
                           "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                          "dtype": "f32", "data": "synthetic", "config": config_block(cfg, args, world),
+                          "dtype": "f32", "data": "synthetic",
+                          "config": config_block(cfg, args, world, l2=l2_label([8 * cfg.params])),
                           "roofline": {"bound": "hbm", "kernel": "merge_kernel", "achieved": gbs,
                                        "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                                        "traffic": None},
@@ -764,6 +833,19 @@ def main():
         e2e_streamed = streamed_leg(cfg, args, world, stream, host_grads=True,
                                     steps=args.e2e_steps)
 
+    # ---- the whole model streamed (TinyLlama-1.1B shape, 201 tensors in 24 units,
+    # K = 4, states in pinned host RAM): the streamed path at model scale
+    whole = None
+    if not args.no_e2e and not args.no_whole_model and args.config == 2 and not args.tensors:
+        from adamw_step_gb300.hostmem import mem_available_bytes
+        cfg4 = configs.CONFIGS[4]
+        need = cfg4.params * (16 if q8 else 24) + (8 << 30)
+        if mem_available_bytes() >= need:
+            whole = streamed_leg(cfg4, args, world, stream, host_grads=False, steps=5)
+            whole["workload"] = cfg4.name
+        else:
+            whole = {"skipped": f"needs {need / 2 ** 30:.0f} GiB of host memory"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, info = cpu_oracle_rate(cfg, args.cpu_seconds, os.cpu_count() or 1, q8)
@@ -774,9 +856,10 @@ def main():
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": config_block(cfg, args, world),
+                "config": config_block(cfg, args, world, l2=l2_label(
+                    [k["bytes_per_launch"] for k in kernels.values()])),
                 "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-                "e2e_streamed": e2e_streamed,
+                "e2e_streamed": e2e_streamed, "whole_model_streamed": whole,
                 "gpu_launches": args.steps * (K if fused else K + 1) *
                                 launches_per_call(len(cfg.tensors), q8), "clocks": clk,
                 "kernel_source": kernel_source_hash("q8" if q8 else "fp32")}

@@ -219,7 +219,15 @@ int lema_accum_grad_q8(const lema_grad_q8* grads, int32_t count, void* cuda_stre
 /* The AdamW step of lema_adamw_step on 8-bit states: per element, decode m, v
  * (from its root) and the accumulated grads, run the same fp32 update (same
  * operation order), write master, delta and w_bf16; per block, encode m and
- * sqrt(v) again.  Same hyperparameter rules and errors as lema_adamw_step. */
+ * sqrt(v) again.  Same hyperparameter rules and errors as lema_adamw_step.
+ *
+ * The kernel stages its inputs through shared memory and waits for those copies
+ * with a bounded wait (about a second).  If a wait runs out, the kernel stops early
+ * and the groups it had not finished keep their old outputs.  That is reported the
+ * way CUDA reports errors of asynchronous work: the next lema_adamw_step_q8 call on
+ * the same device that starts after the kernel has finished returns
+ * LEMA_ERR_TIMEOUT and launches nothing (a call after that runs normally), and
+ * lema_kernel_wait_timeouts counts the event.  Expected never to happen. */
 int lema_adamw_step_q8(const lema_tensor_q8* tensors, int32_t count, int64_t step,
                        double lr, double beta1, double beta2, double eps,
                        double weight_decay, int32_t accum_steps, void* cuda_stream);
@@ -333,8 +341,10 @@ int lema_pool_create(int32_t n_slots, int64_t slot_params, lema_pool** out);
  *                   1..K-1 (never written when K == 1), and the next step's k == 1
  *                   starts again from +0.0 without reading it.
  * With two or more slots the three stages of consecutive units overlap: while unit
- * L is computed, unit L+1 is copied in and unit L-1 copied out.  Results are
- * identical, bit for bit, to lema_accum_grad + lema_adamw_step on the same values.
+ * L is computed, unit L+1 is copied in and unit L-1 copied out; a packed unit also
+ * moves in slices (lema_pool_slices), so its own three stages overlap too.  Results
+ * are identical, bit for bit, to lema_accum_grad + lema_adamw_step on the same
+ * values.
  *
  * LEMA_RESIDENT: every field is device memory and `pool` may be NULL; the call is
  * lema_accum_grad (and, when k == K, an in-place lema_adamw_step) on cuda_stream.
@@ -486,7 +496,11 @@ int lema_disk_probe(const char* path, int64_t bytes, int32_t flags, int32_t n_io
 /* Wait on the host, at most timeout_ms milliseconds (polling, never blocking in a
  * driver call), for all work the pool has enqueued.  Returns LEMA_OK, or
  * LEMA_ERR_TIMEOUT if work is still pending (the pool stays usable), or
- * LEMA_ERR_CUDA if that work failed. */
+ * LEMA_ERR_CUDA if that work failed.  Once the work is done it also returns
+ * LEMA_ERR_TIMEOUT (with a message that says so) when an 8-bit step kernel of this
+ * pool gave up waiting for its staged inputs since the last report: the outputs of
+ * that call are then incomplete.  An lema_stream_layers_q8 call that finds such a
+ * report pending returns it instead of enqueueing anything. */
 int lema_pool_sync(lema_pool* pool, int32_t timeout_ms);
 
 /* Make cuda_stream wait (on the device) for all work the pool has enqueued. */
@@ -495,6 +509,27 @@ int lema_pool_wait_stream(lema_pool* pool, void* cuda_stream);
 /* Wait for the pool's work (without a time limit) and free its slots, streams and
  * events.  NULL is a no-op. */
 int lema_pool_destroy(lema_pool* pool);
+
+/* How the pool splits a unit laid out packed (LEMA_UNIT_PACKED): into at most
+ * max_slices (1..8) slices of whole 8192-element chunks, each at least
+ * min_slice_params elements (rounded up to whole chunks).  Each slice's
+ * host-to-device copies, kernel and device-to-host copies run as soon as the same
+ * slice of the stage before is done, so a unit's computation starts once its first
+ * slice has arrived and its results start leaving before it is all computed; the
+ * results are the same, bit for bit, for any slicing.  Units that are not packed
+ * move whole.  Default: 4 slices of at least 8,388,608 elements.  Applies to calls
+ * made after it.  Returns LEMA_OK or LEMA_ERR_ARG. */
+int lema_pool_slices(lema_pool* pool, int32_t max_slices, int64_t min_slice_params);
+
+/* Measurement mode of a pool: with `on` != 0, every later streamed call
+ * (lema_stream_layers, lema_stream_layers_q8 and their disk forms) enqueues its
+ * copies, events and stream ordering exactly as usual but launches no kernel, so
+ * the host buffers receive whatever the slots held, not results.  Timing a step in
+ * this mode against the same step with the kernels shows how much of the streamed
+ * step the kernels add (nothing, when compute is fully hidden behind the copies).
+ * Off (0) by default; never for training.  Waits for the pool's work first.
+ * Returns LEMA_OK, LEMA_ERR_ARG or the error of that wait. */
+int lema_pool_copies_only(lema_pool* pool, int32_t on);
 
 /* Stage tracing of a pool (a timeline without an external profiler).  With
  * tracing on, each host-to-device, compute and device-to-host stage of every unit
@@ -522,9 +557,9 @@ int lema_pool_trace_read(lema_pool* pool, lema_trace_event* out, int32_t max, in
 
 /* *count = the number of bounded waits inside kernels that ran out on the current
  * device since the library was loaded (the 8-bit step stages its inputs through
- * shared memory and waits for those copies at most about a second; a wait that
- * runs out skips the rest of its chunk and is counted here).  Expected 0.  Reads a
- * device counter (synchronous). */
+ * shared memory and waits for those copies at most about a second; a CTA whose wait
+ * runs out stops and is counted here).  Expected 0.  Reads a device counter
+ * (synchronous). */
 int lema_kernel_wait_timeouts(int64_t* count);
 
 /* Message for the calling thread's last failed call ("" if none). */
@@ -533,10 +568,23 @@ const char* lema_last_error(void);
 /* Name of a status code. */
 const char* lema_status_string(int status);
 
-/* Testing hook for failure handling: the next `nth_copy`-th host<->device copy the
- * pool enqueues (1 = the next one) fails with LEMA_ERR_CUDA without calling CUDA;
- * 0 disarms it.  The fault is made on the host; nothing faults on the GPU. */
+/* ------------------------------------------------------------------------------
+ * Test hooks.  For the library's own failure-handling tests only: they make a
+ * failure happen on purpose.  A program that trains or serves never calls them.
+ * ---------------------------------------------------------------------------- */
+
+/* The `nth_copy`-th host<->device copy the pool enqueues from now on (1 = the next
+ * one) fails with LEMA_ERR_CUDA without calling CUDA; 0 disarms it.  The fault is
+ * made on the host; nothing faults on the GPU. */
 void lema_test_fail_copy(int64_t nth_copy);
+
+/* Sets how long the 8-bit step kernel waits for its staged inputs on the current
+ * device before it gives up (limit_ns < 0 restores the default of about a second;
+ * 0 gives up at the first poll that finds the copies still in flight), so that a
+ * test can make that bounded wait run out.  The kernel still lets every copy it
+ * issued land (with its own, fixed bound) before it stops.  Synchronous (a copy to
+ * the device).  Returns LEMA_OK or LEMA_ERR_CUDA. */
+int lema_test_kernel_wait_limit(int64_t limit_ns);
 
 #ifdef __cplusplus
 }

@@ -66,6 +66,29 @@ def test_streamed_small_matches_oracle(host_grads, n_slots, packed):
     sr.close()
 
 
+@pytest.mark.parametrize("host_grads", [False, True], ids=["device-grads", "host-grads"])
+def test_streamed_sliced_units_match_oracle(host_grads):
+    """Packed units split into up to 4 slices of whole chunks (slice boundaries
+    inside tensors and between them): same bits as the oracle."""
+    cfg = small_config(RAGGED, K=3, steps=3, units=ragged_units())
+    sr = StreamedRunner(cfg, DeviceGrads(cfg, pin_host=host_grads), n_slots=2, packed=True)
+    sr.pool.slices(4, 8192)
+    for t in range(cfg.steps):
+        sr.step(t)
+    sr.pool.sync(600_000)
+    assert check_streamed(cfg, sr, oracle_states(cfg), label="sliced") == 0
+    sr.close()
+
+
+def test_pool_slices_argument_checks():
+    pool = Pool(2, 8192)
+    for bad in ((0, 8192), (9, 8192), (4, 0)):
+        with pytest.raises(lema.LemaError) as e:
+            pool.slices(*bad)
+        assert e.value.status == lema.LEMA_ERR_ARG
+    pool.close()
+
+
 def test_streamed_single_micro_step():
     cfg = small_config([4099, 64, 1], K=1, steps=2, units=[0, 1, 1])
     sr = run_streamed(cfg)

@@ -50,6 +50,22 @@ def compare(state, ref, label, tensors=None):
                 f"{label} tensor {j} {f}: first mismatch at byte {np.flatnonzero(~same)[:3]}"
 
 
+@pytest.mark.parametrize("host_grads", [False, True], ids=["device-grads", "host-grads"])
+def test_q8_streamed_sliced_units(host_grads):
+    """Packed 8-bit units split into up to 4 slices of whole chunks: every field
+    bit for bit against the oracle."""
+    cfg = small_config(SIZES, K=3, steps=2, units=UNITS)
+    sr = StreamedRunnerQ8(cfg, DeviceGrads(cfg, pin_host=host_grads), n_slots=2, packed=True)
+    sr.pool.slices(4, 8192)
+    try:
+        for t in range(cfg.steps):
+            sr.step(t)
+        sr.pool.sync(600_000)
+        compare(sr.state, run_config_q8(cfg, fused=True), "q8 sliced")
+    finally:
+        sr.close()
+
+
 @pytest.mark.parametrize("packed", [True, False], ids=["packed", "per-tensor"])
 @pytest.mark.parametrize("K", [1, 2, 3, 4])
 def test_q8_streamed_bit_exact(K, packed):
