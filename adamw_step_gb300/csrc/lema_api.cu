@@ -77,8 +77,21 @@ int make_scalars(int64_t step, double lr, double beta1, double beta2, double eps
     const bool pow2 = (accum_steps & (accum_steps - 1)) == 0;
     s->accum_pow2 = pow2 ? 1 : 0;
     s->inv_accum = pow2 ? 1.0f / float(accum_steps) : 0.0f;
-    s->reserved = 0;
+    s->bc2_rcp = rcp_rn(s->bc2_sqrt);
     return LEMA_OK;
+}
+
+float rcp_rn(float c) {
+    // 1/c in fp64 is within 2^-53 (relative) of the exact reciprocal, and no exact
+    // reciprocal of a 24-bit significand lies that close to a point halfway between
+    // two fp32 numbers, so rounding it to fp32 is already correct; the neighbours are
+    // still compared, exactly (c * r needs 48 bits, so fp64 holds it and 1 - c * r
+    // without error), so that the result does not rest on that argument.
+    float r = float(1.0 / double(c));
+    const float cand[2] = {std::nextafter(r, 0.0f), std::nextafter(r, HUGE_VALF)};
+    for (float x : cand)
+        if (std::fabs(1.0 - double(c) * double(x)) < std::fabs(1.0 - double(c) * double(r))) r = x;
+    return r;
 }
 
 // ------------------------------------------------------ overlap validation ----
@@ -574,6 +587,32 @@ int direct_flag(GaveUpFlag** out) {
 using namespace lema;
 
 extern "C" const char* lema_last_error(void) { return g_err; }
+
+extern "C" int lema_test_divide_by_constant(const float* divisors, int32_t count,
+                                            int64_t* mismatches, int64_t* outside) {
+    g_err[0] = '\0';
+    if (count < 0 || (count > 0 && (!divisors || !mismatches || !outside)))
+        return set_error(LEMA_ERR_ARG, "bad arguments");
+    for (int32_t i = 0; i < count; ++i)
+        if (!(divisors[i] > 0x1p-27f && divisors[i] <= 1.0f))
+            return set_error(LEMA_ERR_ARG, "divisor %d is outside (2^-27, 1]", i);
+    unsigned long long* bad = nullptr;
+    cudaError_t e = cudaMalloc(&bad, 2 * sizeof(unsigned long long) * size_t(count > 0 ? count : 1));
+    if (e != cudaSuccess) return cuda_error(e, "cudaMalloc");
+    e = cudaMemset(bad, 0, 2 * sizeof(unsigned long long) * size_t(count > 0 ? count : 1));
+    for (int32_t i = 0; i < count && e == cudaSuccess; ++i)
+        e = check_div_by_const(divisors[i], rcp_rn(divisors[i]), bad + 2 * i, nullptr);
+    std::vector<unsigned long long> h(2 * size_t(count > 0 ? count : 1));
+    if (e == cudaSuccess)
+        e = cudaMemcpy(h.data(), bad, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+    cudaFree(bad);
+    if (e != cudaSuccess) return cuda_error(e, "division check");
+    for (int32_t i = 0; i < count; ++i) {
+        mismatches[i] = int64_t(h[2 * size_t(i)]);
+        outside[i] = int64_t(h[2 * size_t(i) + 1]);
+    }
+    return LEMA_OK;
+}
 
 extern "C" int lema_test_kernel_wait_limit(int64_t limit_ns) {
     g_err[0] = '\0';

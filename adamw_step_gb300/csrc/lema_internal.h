@@ -79,8 +79,8 @@ struct StepScalars {
     float eps;
     float accum;       // K
     float inv_accum;   // 1/K, exact when K is a power of two
+    float bc2_rcp;     // 1 / bc2_sqrt, correctly rounded (rcp_rn)
     int32_t accum_pow2;
-    int32_t reserved;
 };
 
 // Kernel launchers (lema_kernels.cu; the 8-bit ones are declared in lema_q8.h).
@@ -116,6 +116,8 @@ void clear_error();
 int cuda_error(cudaError_t e, const char* what);
 int make_scalars(int64_t step, double lr, double beta1, double beta2, double eps,
                  double weight_decay, int32_t accum_steps, StepScalars* out);
+// The fp32 reciprocal of a positive normal c, correctly rounded (RN(1/c)).
+float rcp_rn(float c);
 // Validate + build-or-reuse the device table + launch.  Host arrays of descriptors.
 int run_accum(const AccDesc* descs, int32_t count, cudaStream_t stream);
 int run_step(const StepDesc* descs, int32_t count, const StepScalars& s, cudaStream_t stream);

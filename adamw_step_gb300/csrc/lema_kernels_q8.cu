@@ -181,6 +181,24 @@ __device__ __forceinline__ void step_scales(float amax, float rmax, int lane, fl
     *r_inv = *r_scale == 0.f ? 0.f : ri;
 }
 
+// x / c rounded to nearest even, for the per-call constant c = sqrt(1 - beta2^t)
+// given rc = RN(1/c), by Markstein's method (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1),
+// 1990): q0 = RN(x * rc) lies within one ulp of x/c, so the remainder x - c*q0 is
+// an fp32 number that one fused multiply-add yields exactly, and RN(q0 + rem * rc)
+// is then RN(x/c) -- the same result as an IEEE division, in three operations
+// instead of a full divide.  It holds while nothing underflows or overflows: for
+// x = 0, for 2^-100 <= x <= 2^64 (x/c and the remainder stay normal, since
+// 2^-27 < c <= 1) and, fixed up below, for x = inf.  Here x = sqrt(v), which is
+// never subnormal (the square root of the smallest positive fp32 number is 2^-74.5)
+// and never above 2^64 (the square root of the largest).  NaN stays NaN.
+__device__ __forceinline__ float div_by_const(float x, float c, float rc) {
+    const float q0 = __fmul_rn(x, rc);
+    const float rem = __fmaf_rn(-c, q0, x);
+    const float q = __fmaf_rn(rem, rc, q0);
+    return (x == 0.f || fabsf(x) == __int_as_float(0x7f800000)) ? q0 : q;   // +-0, +-inf
+}
+
 // The fp32 update on decoded states, as adamw_elem, also returning sqrt(v).
 template <bool kPow2>
 __device__ __forceinline__ void adamw_elem_q8(const StepScalars& s, float sum, float orig,
@@ -192,7 +210,7 @@ __device__ __forceinline__ void adamw_elem_q8(const StepScalars& s, float sum, f
     const float v_old = __fmul_rn(r_old, r_old);
     const float v = __fadd_rn(__fmul_rn(s.beta2, v_old), __fmul_rn(s.omb2, __fmul_rn(g, g)));
     root_v = __fsqrt_rn(v);
-    const float den = __fadd_rn(__fdiv_rn(root_v, s.bc2_sqrt), s.eps);
+    const float den = __fadd_rn(div_by_const(root_v, s.bc2_sqrt, s.bc2_rcp), s.eps);
     wn = __fsub_rn(wn, __fmul_rn(s.step_size, __fdiv_rn(m, den)));
     w = wn;
     delta = __fsub_rn(wn, orig);
@@ -832,6 +850,40 @@ cudaError_t launch_step_q8_v(const StepDescQ8* host_descs, int32_t count, const 
         else
             adamw_q8_kernel_v<false, kValueTableMax><<<grid, kThreads, kStepSmem, stream>>>(t, chunks, n_groups, s, gave_up);
     }
+    return cudaGetLastError();
+}
+
+namespace {
+
+// Every x >= 0 from bit pattern `first` on (grid-stride), div_by_const against the
+// IEEE division; counts mismatches inside the domain div_by_const is used on (x = 0,
+// 2^-100 <= x <= 2^64, inf, NaN) and, separately, outside it (subnormal or tiny x,
+// and finite x above 2^64, where x/c may overflow).
+__global__ void check_div_by_const_kernel(float c, float rc, uint32_t first, uint32_t last,
+                                          unsigned long long* bad) {
+    unsigned long long in_dom = 0, out_dom = 0;
+    for (uint64_t b = first + uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; b <= last;
+         b += uint64_t(gridDim.x) * blockDim.x) {
+        const float x = __uint_as_float(uint32_t(b));
+        const float want = __fdiv_rn(x, c), got = div_by_const(x, c, rc);
+        const bool same = __float_as_uint(want) == __float_as_uint(got) ||
+                          (want != want && got != got);
+        if (!same) {
+            const bool tiny = x != 0.f && x < 0x1p-100f;
+            const bool huge = x > 0x1p64f && x <= __int_as_float(0x7f7fffff);
+            if (tiny || huge) ++out_dom;
+            else ++in_dom;
+        }
+    }
+    if (in_dom) atomicAdd(&bad[0], in_dom);
+    if (out_dom) atomicAdd(&bad[1], out_dom);
+}
+
+}  // namespace
+
+cudaError_t check_div_by_const(float c, float rc, unsigned long long* bad_dev,
+                               cudaStream_t stream) {
+    check_div_by_const_kernel<<<1216, 256, 0, stream>>>(c, rc, 0u, 0x7fffffffu, bad_dev);
     return cudaGetLastError();
 }
 

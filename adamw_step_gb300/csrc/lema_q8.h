@@ -66,6 +66,11 @@ cudaError_t launch_step_q8_v(const StepDescQ8* host_descs, int32_t count, const 
 // Count of kernel-side bounded waits (the staged 8-bit step's mbarrier waits) that
 // ran out since the library was loaded on this device.
 cudaError_t read_wait_timeouts(unsigned long long* out);
+// Test: every x >= 0 through the 8-bit step's division by a per-call constant
+// against the IEEE division; adds the mismatches inside (bad_dev[0]) and outside
+// (bad_dev[1]) its domain.
+cudaError_t check_div_by_const(float c, float rc, unsigned long long* bad_dev,
+                               cudaStream_t stream);
 // The staged 8-bit step's wait limit on the current device (ns < 0: the default).
 cudaError_t set_wait_limit(int64_t ns);
 

@@ -161,6 +161,8 @@ def raw():
     lib.lema_test_fail_copy.argtypes = [c_int64]
     lib.lema_test_fail_copy.restype = None
     lib.lema_test_kernel_wait_limit.argtypes = [c_int64]
+    lib.lema_test_divide_by_constant.argtypes = [ctypes.POINTER(ctypes.c_float), c_int32,
+                                                 ctypes.POINTER(c_int64), ctypes.POINTER(c_int64)]
     for name in ("lema_accum_grad", "lema_adamw_step", "lema_adamw_step_noalloc",
                  "lema_accum_grad_q8", "lema_adamw_step_q8", "lema_merge_delta",
                  "lema_pool_create", "lema_stream_layers", "lema_stream_layers_q8",
@@ -169,7 +171,7 @@ def raw():
                  "lema_stream_layers_disk_q8", "lema_disk_probe", "lema_kernel_wait_timeouts",
                  "lema_pool_sync", "lema_pool_wait_stream", "lema_pool_destroy",
                  "lema_pool_trace", "lema_pool_trace_read", "lema_test_kernel_wait_limit",
-                 "lema_pool_copies_only", "lema_pool_slices"):
+                 "lema_pool_copies_only", "lema_pool_slices", "lema_test_divide_by_constant"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -311,6 +313,17 @@ def lema_test_kernel_wait_limit(limit_ns: int) -> None:
     current device (< 0: the default; 0: give up at the first poll that finds the
     copies in flight)."""
     _check(raw().lema_test_kernel_wait_limit(int(limit_ns)))
+
+
+def lema_test_divide_by_constant(divisors):
+    """Test hook: (mismatches, outside) per divisor of the 8-bit step's division by a
+    per-call constant against the IEEE division, over every x >= 0."""
+    n = len(divisors)
+    d = (ctypes.c_float * max(n, 1))(*[float(x) for x in divisors])
+    bad = (c_int64 * max(n, 1))()
+    out = (c_int64 * max(n, 1))()
+    _check(raw().lema_test_divide_by_constant(d, n, bad, out))
+    return list(bad)[:n], list(out)[:n]
 
 
 def lema_disk_layout(unit_params, q8: bool = False):

@@ -586,6 +586,18 @@ void lema_test_fail_copy(int64_t nth_copy);
  * the device).  Returns LEMA_OK or LEMA_ERR_CUDA. */
 int lema_test_kernel_wait_limit(int64_t limit_ns);
 
+/* The 8-bit step divides sqrt(v) by the per-call constant c = sqrt(1 - beta2^t)
+ * with a reciprocal and two fused multiply-adds (Markstein's method) instead of a
+ * division; this runs that operation on the GPU for every x >= 0 (all 2^31 bit
+ * patterns, inf and NaN included) against the IEEE division, for each of `count`
+ * host divisors in (2^-27, 1].  mismatches[i] counts the differing results where
+ * the step uses the method (x = 0, 2^-100 <= x <= 2^64, inf, NaN; expected 0),
+ * outside[i] those for the x it never meets (subnormal or tiny, and finite x above
+ * 2^64, where the quotient may overflow).  Synchronous; allocates a
+ * small device buffer.  Returns LEMA_OK, LEMA_ERR_ARG or LEMA_ERR_CUDA. */
+int lema_test_divide_by_constant(const float* divisors, int32_t count, int64_t* mismatches,
+                                 int64_t* outside);
+
 #ifdef __cplusplus
 }
 #endif

@@ -152,6 +152,31 @@ def test_q8_tiny_blocks_match_the_oracle():
     assert st.acc_scale[0] == 0 and st.acc_scale[1] > 0
 
 
+def test_division_by_the_per_call_constant_is_exact():
+    """The 8-bit step divides sqrt(v) by c = sqrt(1 - beta2^t) with a correctly
+    rounded reciprocal and two fused multiply-adds (Markstein's method); for every
+    x >= 0 in its domain that must equal the IEEE division: the divisors of steps
+    1..200 for several beta2, the ends of the allowed range, all-ones significands
+    and random divisors."""
+    import math
+    cs = set()
+    for beta2 in (0.999, 0.99, 0.95, 0.9, 0.5, 0.9999):
+        p = 1.0
+        for _ in range(200):
+            p *= beta2                      # fp64, one factor at a time, as the host does
+            cs.add(float(np.float32(math.sqrt(1.0 - p))))
+    edge = [1.0, float(np.nextafter(np.float32(2.0 ** -27), np.float32(1))),
+            float(np.nextafter(np.float32(1), np.float32(0)))]
+    edge += [float(np.float32((2 - 2.0 ** -23) * 2.0 ** -k)) for k in range(1, 28)]
+    rng = np.random.default_rng(3)
+    rand = [float(x) for x in np.float32(2.0 ** rng.uniform(-26.9, 0, 200))]
+    divisors = sorted(c for c in cs | set(edge) | set(rand) if 2.0 ** -27 < c <= 1.0)
+    bad, outside = lema.lema_test_divide_by_constant(divisors)
+    wrong = [(c, b) for c, b in zip(divisors, bad) if b]
+    assert not wrong, f"{len(wrong)} divisors with mismatches, e.g. {wrong[:3]}"
+    assert len(divisors) > 900
+
+
 def test_no_kernel_wait_ran_out():
     """The staged 8-bit step waits (bounded) for its shared-memory copies; no launch
     of an ordinary run gives up."""
