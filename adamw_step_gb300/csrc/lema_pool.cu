@@ -17,11 +17,14 @@
 // so the next unit's host-to-device copy into a slot's input half never races the
 // device-to-host copy out of its output half.
 //
-// A unit laid out packed (LEMA_UNIT_PACKED) is moved in up to kMaxSlices slices of
-// whole chunks: slice q's host-to-device copies, its kernel and its device-to-host
-// copies each start as soon as slice q of the stage before is done, so the first
-// kernel starts after one slice has arrived instead of the whole unit, and the
-// last unit's results start leaving before its last slice is computed.
+// A unit laid out packed (LEMA_UNIT_PACKED) can be moved in up to kMaxSlices slices
+// of whole chunks (lema_pool_slices; whole units by default): slice q's
+// host-to-device copies, its kernel and its device-to-host copies each start as
+// soon as slice q of the stage before is done, so a unit's kernel starts after one
+// slice has arrived instead of the whole unit.  Measured, that does not shorten the
+// streamed steps: their last micro-step sends more bytes to the host than it reads
+// from it, so that tail stays, and with the directions overlapping more each runs
+// slower.
 //
 // Ordering (per slot s, per unit L, per slice q):
 //   H2D(L, q)  (from q = 0: waits step_done[s], the input half free, and the D2H
@@ -126,7 +129,7 @@ struct lema_pool {
     int64_t next_slot = 0;
     GaveUpFlag gave_up;   // set by an 8-bit step kernel of this pool whose wait ran out
     bool copies_only = false;   // measurement mode: no kernels (lema_pool_copies_only)
-    int32_t max_slices = 4;                   // lema_pool_slices
+    int32_t max_slices = 1;                   // lema_pool_slices (default: whole units)
     int64_t min_slice = int64_t(8) << 20;     // elements
     std::mutex mu;
     // Stage tracing (off unless lema_pool_trace enabled it): a timed event pair per

@@ -8,13 +8,18 @@ params, K = 8, all fp32 states resident in HBM).  Metric: optimizer params/s.
 
   value    params x steps / device time, inputs resident in HBM (CUDA events,
            barrier + synchronize on both sides, max over ranks)
-  e2e      the same metric through the streamed entry point with every buffer in
-           pinned host memory: per step the K micro-batch grads and the fp32
-           master/m/v/acc and bf16 orig go host -> device and master/m/v, delta,
-           w_bf16 and the partial accumulators come back, all inside the timed region
+  e2e      the same metric through the public calls with host buffers: every
+           micro-step's bf16 grads come from pinned host memory and the step's bf16
+           working weights go back to it, copies inside the timed region; the
+           optimizer states stay resident in HBM, as the workload has them
   roofline the dominant kernel's algorithmic bytes per launch / its CUDA-event
            duration, against the measured HBM copy bandwidth
   cpu_baseline  the CPU oracle on this machine's host cores, on a bounded sample
+  e2e_streamed, whole_model_streamed
+           the same path with every state in pinned host RAM, streamed through
+           the slot pool (the 268M-param set with host grads; the TinyLlama-1.1B
+           whole model), against the host link; each carries compute_hidden, the
+           same steps timed again with the pool's copies-only mode (no kernels)
 
 `--impl reference` times the CPU oracle as the reference arm (no GPU work).
 Multi-GPU (torchrun): every rank runs its own replica (the step has no exchange),
@@ -76,6 +81,11 @@ def parse():
                    help="time lema_merge_delta (bf16(base + delta)) on the workload's tensors")
     p.add_argument("--trace-out", default="",
                    help="streamed legs: record the pool's stage trace and write it (JSON) here")
+    p.add_argument("--slices", type=int, default=0,
+                   help="streamed legs: split each packed unit into at most this many slices "
+                        "(lema_pool_slices; 0: the pool's default, whole units)")
+    p.add_argument("--min-slice", type=int, default=8 << 20,
+                   help="streamed legs with --slices: the smallest slice, in elements")
     p.add_argument("--no-hidden", action="store_true",
                    help="streamed legs: skip the copies-only steps that show whether the "
                         "compute is hidden behind the copies")
@@ -387,6 +397,8 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
     q8 = getattr(args, "q8", False)
     peaks = host_link_peaks(1 << 30, 3)
     sr = (StreamedRunnerQ8 if q8 else StreamedRunner)(cfg, DeviceGrads(cfg, pin_host=host_grads))
+    if getattr(args, "slices", 0):
+        sr.pool.slices(args.slices, args.min_slice)
     huge = anon_huge_bytes()
     for t in range(warmup):
         sr.step(t, stream)
@@ -430,6 +442,8 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
            # states were allocated (the rest uses base pages)
            "host_state_bytes": sr.state.pinned.nbytes, "anon_huge_page_bytes": huge,
            "compute_hidden": hidden,
+           "slices": {"max": getattr(args, "slices", 0) or "pool default (1: whole units)",
+                      "min_params": getattr(args, "min_slice", 8 << 20)},
            "path": f"lema_stream_layers{'_q8' if q8 else ''}, {cfg.n_slots} VRAM slots, "
                    f"3 streams, {'8-bit' if q8 else 'fp32'} states "
                    f"{'and bf16 grads ' if host_grads else ''}in pinned host RAM"}

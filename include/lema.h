@@ -517,8 +517,8 @@ int lema_pool_destroy(lema_pool* pool);
  * slice of the stage before is done, so a unit's computation starts once its first
  * slice has arrived and its results start leaving before it is all computed; the
  * results are the same, bit for bit, for any slicing.  Units that are not packed
- * move whole.  Default: 4 slices of at least 8,388,608 elements.  Applies to calls
- * made after it.  Returns LEMA_OK or LEMA_ERR_ARG. */
+ * move whole.  Default: 1 (whole units; minimum slice 8,388,608 elements when
+ * raised).  Applies to calls made after it.  Returns LEMA_OK or LEMA_ERR_ARG. */
 int lema_pool_slices(lema_pool* pool, int32_t max_slices, int64_t min_slice_params);
 
 /* Measurement mode of a pool: with `on` != 0, every later streamed call
