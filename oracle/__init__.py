@@ -66,11 +66,11 @@ def load(path: str | None = None):
     lib.oracle_q8_decode_signed.argtypes = [i8p, f32p, i64, f32p]
     lib.oracle_q8_encode_root.argtypes = [f32p, i64, u8p, f32p]
     lib.oracle_q8_decode_root.argtypes = [u8p, f32p, i64, f32p]
-    lib.oracle_accum_q8.argtypes = [i8p, f32p, u16p, i64, ctypes.c_int]
+    lib.oracle_accum_q8.argtypes = [i8p, f32p, u16p, i64, ctypes.c_int, ctypes.c_int]
     lib.oracle_merge_delta.argtypes = [u16p, f32p, i64, u16p]
     lib.oracle_adamw_step_q8.argtypes = [i64, f32p, i8p, f32p, u8p, f32p, i8p, f32p, u16p, u16p,
                                          f32p, i8p, f32p, u8p, f32p, f32p, u16p,
-                                         ctypes.POINTER(OracleScalars)]
+                                         ctypes.POINTER(OracleScalars), ctypes.c_int]
     if path is None:
         _lib = lib
     return lib
@@ -201,7 +201,8 @@ class Oracle:
 
     def accum_q8(self, st: "OracleStateQ8", g_bf16, first: bool) -> None:
         self.lib.oracle_accum_q8(_i8(st.acc_q), _f32(st.acc_scale),
-                                 _u16(np.ascontiguousarray(g_bf16)), st.acc_q.size, int(first))
+                                 _u16(np.ascontiguousarray(g_bf16)), st.acc_q.size, int(first),
+                                 self.threads)
 
     def adamw_step_q8(self, st: "OracleStateQ8", step: int, hp: "Hyper", grad_last=None,
                       use_acc=True) -> None:
@@ -218,7 +219,7 @@ class Oracle:
             n, _f32(st.master), _i8(st.m_q), _f32(st.m_scale), _u8(st.r_q), _f32(st.r_scale),
             _i8(st.acc_q) if use_acc else None, _f32(st.acc_scale) if use_acc else None, gl,
             _u16(st.orig), _f32(st.master), _i8(m_q), _f32(m_s), _u8(r_q), _f32(r_s),
-            _f32(st.delta), _u16(st.w), ctypes.byref(s))
+            _f32(st.delta), _u16(st.w), ctypes.byref(s), self.threads)
         st.m_q, st.m_scale, st.r_q, st.r_scale = m_q, m_s, r_q, r_s
 
 

@@ -292,12 +292,15 @@ void oracle_q8_decode_root(const uint8_t* c, const float* scale, int64_t n, floa
 }
 
 /* One micro-step into an 8-bit accumulator: per block, decode (or start from +0
- * when first != 0), add the fp32 grads, encode again. */
+ * when first != 0), add the fp32 grads, encode again.  Blocks are independent; the
+ * OpenMP pragma only splits the block loop over `threads` host cores. */
 void oracle_accum_q8(int8_t* acc_q, float* acc_scale, const uint16_t* g_bf16, int64_t n,
-                     int first)
+                     int first, int threads)
 {
-    float tmp[Q8_BLOCK];
-    for (int64_t b = 0; b < q8_blocks(n); ++b) {
+    const int64_t n_blocks = q8_blocks(n);
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1)
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        float tmp[Q8_BLOCK];
         int64_t lo = b * Q8_BLOCK, nb = n - lo < Q8_BLOCK ? n - lo : Q8_BLOCK;
         for (int64_t i = 0; i < nb; ++i) {
             float a = first ? 0.0f : (float)acc_q[lo + i] * acc_scale[b];
@@ -311,7 +314,8 @@ void oracle_accum_q8(int8_t* acc_q, float* acc_scale, const uint16_t* g_bf16, in
  * accumulated grads, run the fp32 update of oracle_adamw_step element by element,
  * encode m and sqrt(v) again per block.  When grad_last is given it is the K-th
  * micro-batch grad, added to the decoded accumulator (acc_q may then be NULL for
- * K = 1); the accumulator itself is not written. */
+ * K = 1); the accumulator itself is not written.  Blocks are independent; the
+ * OpenMP pragma only splits the block loop over `threads` host cores. */
 void oracle_adamw_step_q8(int64_t n, const float* master_in,
                           const int8_t* m_q_in, const float* m_scale_in,
                           const uint8_t* r_q_in, const float* r_scale_in,
@@ -319,15 +323,18 @@ void oracle_adamw_step_q8(int64_t n, const float* master_in,
                           const uint16_t* grad_last, const uint16_t* orig_bf16,
                           float* master_out, int8_t* m_q_out, float* m_scale_out,
                           uint8_t* r_q_out, float* r_scale_out,
-                          float* delta, uint16_t* w_bf16, const oracle_scalars* s)
+                          float* delta, uint16_t* w_bf16, const oracle_scalars* s,
+                          int threads)
 {
-    float m_new[Q8_BLOCK], r_new[Q8_BLOCK];
     const float decay = s->decay;
     const float b1 = s->beta1, omb1 = s->one_minus_beta1;
     const float b2 = s->beta2, omb2 = s->one_minus_beta2;
     const float step_size = s->step_size, bc2_sqrt = s->bc2_sqrt;
     const float eps = s->eps, K = s->accum_steps;
-    for (int64_t b = 0; b < q8_blocks(n); ++b) {
+    const int64_t n_blocks = q8_blocks(n);
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1)
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        float m_new[Q8_BLOCK], r_new[Q8_BLOCK];
         int64_t lo = b * Q8_BLOCK, nb = n - lo < Q8_BLOCK ? n - lo : Q8_BLOCK;
         for (int64_t j = 0; j < nb; ++j) {
             int64_t i = lo + j;

@@ -93,14 +93,14 @@ def test_q8_streamed_host_grads_three_slots_matches_resident():
         sr.close()
 
 
-def test_q8_streamed_268m_sampled():
-    """The 268M-parameter streamed workload (16 units, K=8) with 8-bit states:
-    tensors 0, 7 and 15 against the oracle on every element."""
+def test_q8_streamed_268m_full():
+    """The 268M-parameter streamed workload (4 units of 4 tensors, K=8) with 8-bit
+    states: every element of every tensor against the oracle."""
+    from oracle_cache import oracle_states_q8
     cfg = configs.CONFIGS[3]
     sr = run_streamed(cfg)
     try:
-        compare(sr.state, run_config_q8(cfg, tensors=[0, 7, 15], fused=True), "q8 config 3",
-                tensors=[0, 7, 15])
+        compare(sr.state, oracle_states_q8(cfg, fused=True), "q8 config 3")
     finally:
         sr.close()
 
