@@ -547,8 +547,12 @@ void gave_up_flag_free(GaveUpFlag* f) {
 }
 
 int gave_up_take(const GaveUpFlag& f, const char* where) {
-    if (!f.host || *f.host == 0u) return LEMA_OK;
-    *f.host = 0u;
+    if (!f.host) return LEMA_OK;
+    // An atomic exchange, so that a kernel still running that sets the word between
+    // a read and a reset on the host is not lost: its 1 stays for the next check.
+    const unsigned int was =
+        __atomic_exchange_n(const_cast<unsigned int*>(f.host), 0u, __ATOMIC_ACQ_REL);
+    if (was == 0u) return LEMA_OK;
     return set_error(LEMA_ERR_TIMEOUT,
                      "%s: an 8-bit step kernel gave up waiting for its staged inputs (see "
                      "lema_kernel_wait_timeouts); the groups it had not finished kept their old "

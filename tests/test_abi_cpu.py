@@ -99,6 +99,13 @@ def test_pool_validation_before_cuda(lib):
     Q[0].count = 1
     assert lib.lema_stream_layers_q8(None, Q, 1, 1, ctypes.byref(hp), 1, None) == -1
     assert lib.lema_pool_destroy(None) == 0
+    assert lib.lema_pool_slices(None, 4, 8192) == -1
+    assert lib.lema_pool_copies_only(None, 1) == -1
+    # the division check takes divisors in (2^-27, 1] only (rejected before any CUDA call)
+    d = (ctypes.c_float * 1)(2.0)
+    bad, out = (ctypes.c_int64 * 1)(), (ctypes.c_int64 * 1)()
+    assert lib.lema_test_divide_by_constant(d, 1, bad, out) == -1
+    assert lib.lema_test_divide_by_constant(d, -1, bad, out) == -1
 
 
 def test_struct_layouts_match_header(tmp_path):

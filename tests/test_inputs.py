@@ -70,3 +70,13 @@ def test_kernel_hash_ignores_comments_only():
     assert bench._code_only(a) == bench._code_only('/* doc */ int  f(int x)\n{ return x + 1; }')
     assert bench._code_only(a) != bench._code_only(a.replace("+ 1", "+ 2"))
     assert bench._code_only('s = "a // b";') == 's="a // b";'
+
+
+def test_bench_l2_label_follows_the_bytes_per_launch():
+    """bench.py labels a workload by whether its launches can be served from the
+    129 MB L2: every launch above it, every launch within it, or some of each."""
+    import bench
+    assert bench.l2_label([1.6e9, 10.2e9]).startswith("inputs larger than L2")
+    assert "within the 129 MB L2" in bench.l2_label([6e6, 10e6])
+    mixed = bench.l2_label([27e6, 45e6, 173e6])
+    assert "partly L2-served" in mixed and "27-173 MB" in mixed
