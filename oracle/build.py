@@ -3,7 +3,8 @@
 Plain gcc, no fast-math, no contraction into fused multiply-add (GCC contracts by
 default on aarch64), no auto-vectorisation, so that every fp32 operation in
 ``lema_oracle.c`` is one IEEE operation rounded to nearest even.  OpenMP is used
-when the compiler has it; it only splits the element loop for the timed baseline.
+when the compiler has it; it only splits the loops over independent elements (or
+8-bit blocks) across threads.
 """
 from __future__ import annotations
 

@@ -22,9 +22,10 @@
  * nearest even, no fused multiply-add, subnormals kept).
  *
  * Build: plain C, -O2 -ffp-contract=off -fno-fast-math -fno-tree-vectorize.
- * The optional OpenMP pragma only splits the element loop across threads for the
- * timed CPU baseline; every element is independent, so results are identical for
- * any thread count.
+ * The optional OpenMP pragmas only split the element loops (and, for 8-bit
+ * states, the loops over 256-element blocks) across threads, for the timed CPU
+ * baseline and to check whole workloads in reasonable time; every element (every
+ * block) is independent, so results are identical for any thread count.
  */
 #include <stdint.h>
 #include <string.h>
