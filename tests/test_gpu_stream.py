@@ -80,6 +80,30 @@ def test_streamed_sliced_units_match_oracle(host_grads):
     sr.close()
 
 
+def test_copies_only_mode_leaves_the_pool_usable():
+    """The measurement mode enqueues a streamed step's copies without kernels (its
+    host outputs are then slot contents, not results); switched off again, the same
+    pool runs a fresh state to the oracle's bits."""
+    cfg = small_config(RAGGED, K=2, steps=2, units=ragged_units())
+    sr = StreamedRunner(cfg, DeviceGrads(cfg))
+    lema.lema_pool_copies_only(sr.pool.handle, True)
+    try:
+        for t in range(cfg.steps):
+            sr.step(t)
+        sr.pool.sync(60_000)
+    finally:
+        lema.lema_pool_copies_only(sr.pool.handle, False)
+    fresh = StreamedRunner(cfg, DeviceGrads(cfg))
+    fresh.pool.close()
+    fresh.pool = sr.pool
+    for t in range(cfg.steps):
+        fresh.step(t)
+    fresh.pool.sync(60_000)
+    assert check_streamed(cfg, fresh, oracle_states(cfg), label="after copies-only") == 0
+    fresh.state.close()
+    sr.close()
+
+
 def test_pool_slices_argument_checks():
     pool = Pool(2, 8192)
     for bad in ((0, 8192), (9, 8192), (4, 0)):
