@@ -84,6 +84,8 @@ def parse():
     p.add_argument("--slices", type=int, default=0,
                    help="streamed legs: split each packed unit into at most this many slices "
                         "(lema_pool_slices; 0: the pool's default, whole units)")
+    p.add_argument("--slots", type=int, default=0,
+                   help="streamed legs: VRAM slots of the pool (0: the workload's own, 2)")
     p.add_argument("--min-slice", type=int, default=8 << 20,
                    help="streamed legs with --slices: the smallest slice, in elements")
     p.add_argument("--no-hidden", action="store_true",
@@ -396,7 +398,8 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
     from adamw_step_gb300.runner import DeviceGrads, StreamedRunner, StreamedRunnerQ8
     q8 = getattr(args, "q8", False)
     peaks = host_link_peaks(1 << 30, 3)
-    sr = (StreamedRunnerQ8 if q8 else StreamedRunner)(cfg, DeviceGrads(cfg, pin_host=host_grads))
+    sr = (StreamedRunnerQ8 if q8 else StreamedRunner)(cfg, DeviceGrads(cfg, pin_host=host_grads),
+                                                      n_slots=getattr(args, "slots", 0) or None)
     if getattr(args, "slices", 0):
         sr.pool.slices(args.slices, args.min_slice)
     huge = anon_huge_bytes()
@@ -444,7 +447,8 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
            "compute_hidden": hidden,
            "slices": {"max": getattr(args, "slices", 0) or "pool default (1: whole units)",
                       "min_params": getattr(args, "min_slice", 8 << 20)},
-           "path": f"lema_stream_layers{'_q8' if q8 else ''}, {cfg.n_slots} VRAM slots, "
+           "path": f"lema_stream_layers{'_q8' if q8 else ''}, "
+                   f"{getattr(args, 'slots', 0) or cfg.n_slots} VRAM slots, "
                    f"3 streams, {'8-bit' if q8 else 'fp32'} states "
                    f"{'and bf16 grads ' if host_grads else ''}in pinned host RAM"}
     sr.close()
