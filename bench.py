@@ -853,8 +853,10 @@ def main():
 
     # ---- the whole model streamed (TinyLlama-1.1B shape, 201 tensors in 24 units,
     # K = 4, states in pinned host RAM): the streamed path at model scale
+    # (one GPU only: N replicas would each pin 26 GB of host memory at once)
     whole = None
-    if not args.no_e2e and not args.no_whole_model and args.config == 2 and not args.tensors:
+    if not args.no_e2e and not args.no_whole_model and args.config == 2 and not args.tensors \
+            and world == 1:
         from adamw_step_gb300.hostmem import mem_available_bytes
         cfg4 = configs.CONFIGS[4]
         need = cfg4.params * (16 if q8 else 24) + (8 << 30)
