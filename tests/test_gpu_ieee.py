@@ -24,7 +24,7 @@ import torch
 
 import oracle
 from adamw_step_gb300 import lema
-from adamw_step_gb300.state import HostState, Layers, Pool
+from adamw_step_gb300.state import DeviceStateQ8, HostState, Layers, Pool
 from adamw_step_gb300.lema import LemaHparams
 from gpu_common import ensure_library
 from parity import check_tensor
@@ -211,3 +211,51 @@ def test_streamed_special_values():
         assert sum(rep.values()) == 0, rep
     pool.close()
     st.close()
+
+
+# 8-bit states must stay finite (a NaN or an infinity has no code), so their case
+# keeps every value finite: tiny and subnormal grads and weights, signed zeros, and
+# grads as large as 2^61, whose square (2^122) is still an fp32 number.
+BF16_FINITE = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x0080, 0x8080, 0x1E80, 0x9E80,
+                        0x3A83, 0xBA83, 0x5B00, 0xDB00, 0x5E00, 0xDE00], dtype=np.uint16)
+
+
+def _mix_bf16_finite(rng, n, scale, frac=0.5):
+    x = torch.from_numpy((rng.standard_normal(n) * scale).astype(np.float32))
+    h = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    pick = rng.random(n) < frac
+    h[pick] = BF16_FINITE[rng.integers(0, BF16_FINITE.size, int(pick.sum()))]
+    return h
+
+
+@pytest.mark.parametrize("K", [2, 3])
+def test_q8_step_tiny_subnormal_and_large_values(K):
+    """The 8-bit accumulate and step (fused form) on weights and grads that include
+    bf16 subnormals, +-0, 2^-66 and values up to 2^61 (0x5E00: g^2 stays finite):
+    codes, block scales, master, delta and bf16 weight bit for bit against the
+    oracle's 8-bit form, two steps."""
+    n = 5 * 2048 + 300                      # staged groups and a ragged end
+    rng = np.random.default_rng(40 + K)
+    w0 = _mix_bf16_finite(rng, n, 0.02)
+    grads = [[_mix_bf16_finite(rng, n, 1e-3) for _ in range(K)] for _ in range(2)]
+    st = DeviceStateQ8([torch.from_numpy(w0.view(np.int16).copy()).view(torch.bfloat16)])
+    dg = [[_dev_u16(g) for g in row] for row in grads]
+    h = oracle.Hyper(accum_steps=K)
+    for t in range(2):
+        for k in range(K - 1):
+            lema.lema_accum_grad_q8(st.grad_descs([dg[t][k]], first=(k == 0)))
+        d = st.tensor_desc(0, grad=dg[t][K - 1], flags=lema.LEMA_STEP_KEEP_ACC)
+        lema.lema_adamw_step_q8([d], t + 1, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, K)
+    torch.cuda.synchronize()
+    orc = oracle.Oracle()
+    ref = oracle.OracleStateQ8(w0, orc)
+    for t in range(2):
+        for k in range(K - 1):
+            orc.accum_q8(ref, grads[t][k], first=(k == 0))
+        orc.adamw_step_q8(ref, t + 1, h, grad_last=grads[t][K - 1])
+    got = st.numpy_views(0)
+    for f in ("master", "delta", "w", "m_q", "m_scale", "r_q", "r_scale", "acc_q", "acc_scale"):
+        a, b = got[f], getattr(ref, f)
+        same = a.view(np.uint8) == b.view(np.uint8)
+        assert same.all(), f"K={K} {f}: first mismatch at byte {np.flatnonzero(~same)[:3]}"
+    assert np.isfinite(ref.master).all() and np.isfinite(ref.r_scale).all()
