@@ -13,8 +13,10 @@ never leave the normal range, so these cases feed the kernels inputs that do:
 * beta1 = 0, lr = 0, a subnormal eps, K = 3 (divide) and K = 4 (the exact
   reciprocal multiply), steps 1 and 7.
 
-Every field must equal the oracle's bits (NaN compared as NaN).  A build that
-flushed subnormals (``-ftz=true``) or contracted into FMA would fail here.
+The 8-bit path gets the finite part of this (its states must be finite) and the
+serving merge bf16(base + delta) the whole of it.  Every field must equal the
+oracle's bits (NaN compared as NaN).  A build that flushed subnormals
+(``-ftz=true``) or contracted into FMA would fail here.
 """
 from __future__ import annotations
 
@@ -259,3 +261,23 @@ def test_q8_step_tiny_subnormal_and_large_values(K):
         same = a.view(np.uint8) == b.view(np.uint8)
         assert same.all(), f"K={K} {f}: first mismatch at byte {np.flatnonzero(~same)[:3]}"
     assert np.isfinite(ref.master).all() and np.isfinite(ref.r_scale).all()
+
+
+def test_merge_special_values():
+    """bf16(base + delta) with NaN, +-Inf, -0, subnormal and overflowing sums, against
+    the oracle's merge bit for bit (a NaN result is the bf16 pattern 0x7FC0 on both
+    sides); in place and out of place."""
+    rng = np.random.default_rng(77)
+    n = 3 * 8192 + 21
+    base = _mix_bf16(rng, n, 0.02)
+    delta = _mix_f32(rng, n, 1e-4)
+    want = oracle.Oracle().merge_delta(base, delta)
+    for in_place in (False, True):
+        db, dd = _dev_u16(base), _dev_f32(delta)
+        out = db if in_place else torch.zeros(n, dtype=torch.int16, device="cuda")
+        lema.lema_merge_delta([lema.LemaMerge(base_bf16=db.data_ptr(), delta=dd.data_ptr(),
+                                              merged_bf16=out.data_ptr(), n=n)])
+        torch.cuda.synchronize()
+        got = _host(out, u16=True)
+        assert np.array_equal(got, want), f"in_place={in_place}: {np.flatnonzero(got != want)[:5]}"
+    assert (want == 0x7FC0).any() and (want == 0x7F80).any() and (want == 0xFF80).any()
