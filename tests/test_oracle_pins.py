@@ -45,3 +45,32 @@ def test_scalars_reject_out_of_domain(orc):
         kw.update(bad)
         with pytest.raises(ValueError):
             orc.scalars(**kw)
+
+
+def test_threads_do_not_change_the_oracle():
+    """The OpenMP loops only split independent elements (8-bit: independent blocks)
+    across threads: one thread and four give the same bits, fp32 and 8-bit."""
+    import numpy as np
+    rng = np.random.default_rng(9)
+    n = 40_000 + 77
+    w0 = (rng.standard_normal(n).astype(np.float32) * 0.02).view(np.uint32)
+    w0 = ((w0 + 0x7FFF + ((w0 >> 16) & 1)) >> 16).astype(np.uint16)      # bf16 of the draws
+    gs = [((rng.standard_normal(n).astype(np.float32) * 1e-3).view(np.uint32) >> 16)
+          .astype(np.uint16) for _ in range(3)]
+    h = oracle.Hyper(accum_steps=3)
+    out = []
+    for th in (1, 4):
+        o = oracle.Oracle(threads=th)
+        st = oracle.OracleState(w0, o)
+        sq = oracle.OracleStateQ8(w0, o)
+        for t in range(2):
+            for g in gs:
+                o.accum(st.acc, g)
+            o.adamw_step(st, t + 1, h)
+            for k, g in enumerate(gs[:-1]):
+                o.accum_q8(sq, g, first=(k == 0))
+            o.adamw_step_q8(sq, t + 1, h, grad_last=gs[-1])
+        out.append([st.master, st.m, st.v, st.delta, st.w, sq.master, sq.m_q, sq.m_scale,
+                    sq.r_q, sq.r_scale, sq.acc_q, sq.acc_scale, sq.delta, sq.w])
+    for a, b in zip(*out):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
