@@ -199,9 +199,10 @@ class Pool:
 
 
 def slot_params_for(cfg) -> int:
-    """Slot capacity (elements) that fits the largest streaming unit of cfg."""
-    return max(sum(_pad(cfg.tensors[j].numel) for j in cfg.unit_tensors(u))
-               for u in range(cfg.n_units))
+    """Slot capacity (elements) that fits the largest streaming unit of cfg (at least
+    one element: a pool needs a size even when every tensor is empty)."""
+    return max(1, max(sum(_pad(cfg.tensors[j].numel) for j in cfg.unit_tensors(u))
+                      for u in range(cfg.n_units)))
 
 
 Q8_BLOCK = 256

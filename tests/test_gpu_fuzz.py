@@ -1,0 +1,107 @@
+"""Seeded random workloads through the C ABI against the oracle, bit for bit.
+
+Each case draws a tensor count (on both sides of the by-value descriptor table's
+64-tensor limit), ragged sizes (empty tensors included), K, the number of steps,
+the hyperparameters (betas, lr, eps, weight decay inside the method's domain) and
+the form (fused: last grad folded in; unfused: K accumulates, then the step), and
+runs it resident with fp32 states and with 8-bit states, and streamed through a
+pool of two or three slots.  Every field must equal the oracle's bits.  The seeds
+are fixed, so every run checks the same cases.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.runner import run_config, run_config_q8
+from adamw_step_gb300 import configs
+from adamw_step_gb300.runner import DeviceGrads, ResidentRunner, ResidentRunnerQ8, StreamedRunner
+from gpu_common import ensure_library
+from parity import check_tensor, oracle_dict, partial_acc, state_dict
+
+pytestmark = pytest.mark.gpu
+CASES = 12
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    return ensure_library()
+
+
+def draw(seed):
+    rng = np.random.default_rng(1000 + seed)
+    count = int(rng.choice([1, 3, 17, 64, 65, 90]))
+    sizes = []
+    for _ in range(count):
+        kind = rng.integers(0, 4)
+        n = (0 if kind == 0 else int(rng.integers(1, 300)) if kind == 1
+             else int(rng.integers(1, 9000)) if kind == 2 else int(rng.integers(8000, 70_000)))
+        sizes.append(n)
+    K = int(rng.integers(1, 6))
+    steps = int(rng.integers(1, 4))
+    b1 = float(rng.choice([0.0, 0.5, 0.9, 0.95]))
+    b2 = float(rng.choice([0.9, 0.99, 0.999, 0.9999]))
+    lr = float(rng.choice([0.0, 1e-5, 1e-4, 3e-3]))
+    wd = float(rng.choice([0.0, 0.01, 0.1]))
+    eps = float(rng.choice([1e-8, 1e-6, 1e-12]))
+    units = sorted(int(u) for u in rng.integers(0, max(1, count // 4) + 1, size=count))
+    units = [u - units[0] for u in units]
+    remap = {u: i for i, u in enumerate(sorted(set(units)))}
+    units = [remap[u] for u in units]
+    tensors = tuple(configs.TensorSpec(f"f{seed}_{i}", (n,), u)
+                    for i, (n, u) in enumerate(zip(sizes, units)))
+    cfg = configs.scaled(configs.CONFIGS[1], tensors, accum_steps=K, steps=steps,
+                         grad_mode="fresh", name=f"fuzz {seed}",
+                         hyper=configs.Hyper(lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=wd))
+    fused = bool(rng.integers(0, 2))
+    return cfg, fused, int(rng.integers(2, 4))
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_fuzz_resident_fp32(seed):
+    cfg, fused, _ = draw(seed)
+    r = ResidentRunner(cfg, DeviceGrads(cfg), fused=fused)
+    for t in range(cfg.steps):
+        r.step(t)
+    torch.cuda.synchronize()
+    ref = run_config(cfg)
+    for j, st in ref.items():
+        want = oracle_dict(st)
+        if fused:
+            want = dict(want, acc=partial_acc(cfg, j))
+        rep = check_tensor(state_dict(r.state, j), want, f"seed {seed} tensor {j}")
+        assert sum(rep.values()) == 0, rep
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_fuzz_resident_q8(seed):
+    cfg, fused, _ = draw(seed)
+    r = ResidentRunnerQ8(cfg, DeviceGrads(cfg), fused=fused)
+    for t in range(cfg.steps):
+        r.step(t)
+    torch.cuda.synchronize()
+    for j, st in run_config_q8(cfg, fused=fused).items():
+        got = r.state.numpy_views(j)
+        for f in ("master", "delta", "w", "m_q", "m_scale", "r_q", "r_scale", "acc_q",
+                  "acc_scale"):
+            same = got[f].view(np.uint8) == getattr(st, f).view(np.uint8)
+            assert same.all(), f"seed {seed} tensor {j} {f}: byte {np.flatnonzero(~same)[:3]}"
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_fuzz_streamed_fp32(seed):
+    cfg, _, n_slots = draw(seed)
+    sr = StreamedRunner(cfg, DeviceGrads(cfg), n_slots=n_slots)
+    try:
+        for t in range(cfg.steps):
+            sr.step(t)
+        sr.pool.sync(120_000)
+        ref = run_config(cfg)
+        for j, st in ref.items():
+            # the host accumulator keeps micro-steps 1..K-1 of the last step
+            want = dict(oracle_dict(st), acc=partial_acc(cfg, j))
+            rep = check_tensor(state_dict(sr.state, j), want, f"seed {seed} tensor {j}")
+            assert sum(rep.values()) == 0, rep
+    finally:
+        sr.close()
