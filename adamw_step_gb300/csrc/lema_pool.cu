@@ -118,6 +118,7 @@ struct lema_pool {
     int device = 0;
     int n_slots = 0;
     int64_t slot_params = 0;
+    int64_t slot_bytes = 0;
     void* slab = nullptr;
     std::vector<Slot> slots;
     cudaStream_t h2d = nullptr, cmp = nullptr, d2h = nullptr;
@@ -334,6 +335,10 @@ int check_streamed_unit(const lema_layer& ly, int32_t L, int32_t k, bool final_s
 
 }  // namespace
 
+namespace {
+int64_t carved_q8_bytes(int64_t P);   // the 8-bit slot layout (below)
+}  // namespace
+
 // =================================================================== C ABI ====
 
 extern "C" int lema_pool_create(int32_t n_slots, int64_t slot_params, lema_pool** out) {
@@ -348,7 +353,11 @@ extern "C" int lema_pool_create(int32_t n_slots, int64_t slot_params, lema_pool*
     p->n_slots = n_slots;
     p->slot_params = round_up(slot_params, 128);
     const int64_t P = p->slot_params;
-    const size_t slot_bytes = size_t(P) * 38;
+    // 38 bytes per element hold the fp32 layout; the 8-bit carving (its fields each
+    // rounded up to 256 bytes) needs a little more than its 24 bytes per element,
+    // which only tiny slots notice.
+    const size_t slot_bytes = size_t(std::max<int64_t>(P * 38, carved_q8_bytes(P)));
+    p->slot_bytes = int64_t(slot_bytes);
     e = cudaMalloc(&p->slab, slot_bytes * size_t(n_slots));
     if (e != cudaSuccess) {
         p->slab = nullptr;
@@ -866,7 +875,8 @@ SlotQ8 carve_q8(const Slot& s, int64_t P) {
     return q;
 }
 
-// Bytes carve_q8 uses for a slot of P elements (must not exceed the slot's 38 P).
+// Bytes carve_q8 uses for a slot of P elements (the pool sizes each slot for the
+// larger of this and the fp32 layout's 38 P).
 int64_t carved_q8_bytes(int64_t P) {
     const int64_t nb = (P + kQBlock - 1) / kQBlock;
     auto r = [](int64_t x) { return (x + 255) / 256 * 256; };
@@ -996,7 +1006,7 @@ extern "C" int lema_stream_layers_q8(lema_pool* pool, const lema_layer_q8* layer
 int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, int32_t n_layers,
                                  int32_t micro_step, int32_t K, const StepScalars& s,
                                  cudaStream_t caller, UnitHooks* hooks) {
-    if (carved_q8_bytes(pool->slot_params) > pool->slot_params * 38)
+    if (carved_q8_bytes(pool->slot_params) > pool->slot_bytes)
         return set_error(LEMA_ERR_STATE, "slot too small for the 8-bit layout");
     // A give-up in an earlier call that nobody has synced on yet: report it first.
     LEMA_TRY(gave_up_take(pool->gave_up, "8-bit streamed call (an earlier call of this pool; "

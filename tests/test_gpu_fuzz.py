@@ -4,8 +4,8 @@ Each case draws a tensor count (on both sides of the by-value descriptor table's
 64-tensor limit), ragged sizes (empty tensors included), K, the number of steps,
 the hyperparameters (betas, lr, eps, weight decay inside the method's domain) and
 the form (fused: last grad folded in; unfused: K accumulates, then the step), and
-runs it resident with fp32 states and with 8-bit states, and streamed through a
-pool of two or three slots.  Every field must equal the oracle's bits.  The seeds
+runs it resident and streamed (through a pool of two or three slots), with fp32
+states and with 8-bit states.  Every field must equal the oracle's bits.  The seeds
 are fixed, so every run checks the same cases.
 """
 from __future__ import annotations
@@ -16,12 +16,13 @@ import torch
 
 from oracle.runner import run_config, run_config_q8
 from adamw_step_gb300 import configs
-from adamw_step_gb300.runner import DeviceGrads, ResidentRunner, ResidentRunnerQ8, StreamedRunner
+from adamw_step_gb300.runner import (DeviceGrads, ResidentRunner, ResidentRunnerQ8,
+                                     StreamedRunner, StreamedRunnerQ8)
 from gpu_common import ensure_library
 from parity import check_tensor, oracle_dict, partial_acc, state_dict
 
 pytestmark = pytest.mark.gpu
-CASES = 12
+CASES = 40
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -103,5 +104,23 @@ def test_fuzz_streamed_fp32(seed):
             want = dict(oracle_dict(st), acc=partial_acc(cfg, j))
             rep = check_tensor(state_dict(sr.state, j), want, f"seed {seed} tensor {j}")
             assert sum(rep.values()) == 0, rep
+    finally:
+        sr.close()
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_fuzz_streamed_q8(seed):
+    cfg, _, n_slots = draw(seed)
+    sr = StreamedRunnerQ8(cfg, DeviceGrads(cfg), n_slots=n_slots)
+    try:
+        for t in range(cfg.steps):
+            sr.step(t)
+        sr.pool.sync(120_000)
+        for j, st in run_config_q8(cfg, fused=True).items():
+            got = sr.state.numpy_views(j)
+            for f in ("master", "delta", "w", "m_q", "m_scale", "r_q", "r_scale", "acc_q",
+                      "acc_scale"):
+                same = got[f].view(np.uint8) == getattr(st, f).view(np.uint8)
+                assert same.all(), f"seed {seed} tensor {j} {f}: byte {np.flatnonzero(~same)[:3]}"
     finally:
         sr.close()
