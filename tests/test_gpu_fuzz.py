@@ -124,3 +124,46 @@ def test_fuzz_streamed_q8(seed):
                 assert same.all(), f"seed {seed} tensor {j} {f}: byte {np.flatnonzero(~same)[:3]}"
     finally:
         sr.close()
+
+
+@pytest.mark.parametrize("seed", range(0, CASES, 2))
+def test_fuzz_noalloc_out_of_place_and_shards(seed):
+    """The same random workloads, unfused, through three other forms of the step,
+    each against the oracle: lema_adamw_step_noalloc in place, lema_adamw_step out of
+    place (fresh outputs every step, the inputs then copied forward), and the step
+    sharded over 2-5 "ranks" (each an aligned element range of every tensor, run one
+    after another)."""
+    from adamw_step_gb300 import inputs, lema
+    from adamw_step_gb300.shard import shard_bounds, shard_grad, shard_tensor
+    from adamw_step_gb300.state import DeviceState
+    cfg, _, _ = draw(seed)
+    world = 2 + seed % 4
+    hp, K = cfg.hyper, cfg.accum_steps
+    args = lambda t: (t + 1, hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, K)  # noqa: E731
+    w0 = [inputs.w0_bf16(cfg, j) for j in range(len(cfg.tensors))]
+    a, b, c = DeviceState(w0), DeviceState(w0), DeviceState(w0)
+    n = [x.numel for x in cfg.tensors]
+    for t in range(cfg.steps):
+        grads = [[inputs.fresh_grad(cfg, j, t, k).cuda() for j in range(len(n))] for k in range(K)]
+        for st in (a, b, c):
+            for k in range(K):
+                lema.lema_accum_grad(st.grad_descs(grads[k], first=k == 0))
+        lema.lema_adamw_step_noalloc(a.tensor_descs(), *args(t))
+        outs = [[torch.empty_like(x["master"]) for _ in range(3)] for x in b.tensors]
+        lema.lema_adamw_step([b.tensor_desc(j, out_of_place=outs[j]) for j in range(len(n))],
+                             *args(t))
+        for rank in range(world):
+            bounds = [shard_bounds(x, rank, world) for x in n]
+            d = c.tensor_descs()
+            lema.lema_adamw_step([shard_tensor(d[j], *bounds[j]) for j in range(len(n))],
+                                 *args(t))
+        torch.cuda.synchronize()
+        for j, x in enumerate(b.tensors):       # out of place: carry the outputs forward
+            for f, o in zip(("master", "m", "v"), outs[j]):
+                x[f].copy_(o)
+            x["acc"].zero_()                    # an out-of-place step leaves acc as it was
+    ref = run_config(cfg)
+    for st, label in ((a, "noalloc"), (b, "out of place"), (c, f"{world} shards")):
+        for j, r in ref.items():
+            rep = check_tensor(state_dict(st, j), oracle_dict(r), f"seed {seed} {label} tensor {j}")
+            assert sum(rep.values()) == 0, rep
