@@ -247,11 +247,38 @@ void note_writer(lema_pool* pool, const void* p, std::vector<size_t>& waits);
 int wait_for_writers(lema_pool* pool, std::vector<size_t>& waits);
 int end_call(lema_pool* pool);
 
-// Host-side checks of one unit for a streamed call; fills grad_on_host per tensor.
+// The residency of a unit's accumulators: every non-empty tensor's accumulator
+// buffers (fp32: acc; 8-bit: codes and scales) in pinned host memory (1) or all in
+// device memory (2).  *kind is 0 on entry and stays 0 for a unit with no data.
+int check_acc_kind(const void* const* bufs, int n_bufs, int32_t L, int32_t j,
+                   std::unordered_map<const void*, int>& kinds, int* kind) {
+    for (int i = 0; i < n_bufs; ++i) {
+        const void* p = bufs[i];
+        if (!p) return set_error(LEMA_ERR_ARG, "unit %d tensor %d: NULL accumulator", L, j);
+        if (!aligned16(p))
+            return set_error(LEMA_ERR_ALIGN, "unit %d tensor %d: accumulator not 16-byte aligned",
+                             L, j);
+        const int k = cached_kind(kinds, p);
+        if (k == 0)
+            return set_error(LEMA_ERR_ARG,
+                             "unit %d tensor %d: accumulator must be pinned host or device memory",
+                             L, j);
+        if (*kind != 0 && k != *kind)
+            return set_error(LEMA_ERR_ARG,
+                             "unit %d tensor %d: a unit's accumulators must all be pinned host "
+                             "memory or all device memory", L, j);
+        *kind = k;
+    }
+    return LEMA_OK;
+}
+
+// Host-side checks of one unit for a streamed call; fills grad_on_host per tensor
+// and *acc_on_device (the unit's accumulators live in device memory).
 int check_streamed_unit(const lema_layer& ly, int32_t L, int32_t k, bool final_step,
                         int64_t slot_params, std::vector<char>& grad_on_host,
-                        std::unordered_map<const void*, int>& kinds) {
+                        std::unordered_map<const void*, int>& kinds, bool* acc_on_device) {
     int64_t need = 0;
+    int acc_kind = 0;
     for (int32_t j = 0; j < ly.count; ++j) {
         const lema_tensor& t = ly.tensors[j];
         if (t.n < 0) return set_error(LEMA_ERR_ARG, "unit %d tensor %d: n must be >= 0", L, j);
@@ -263,7 +290,9 @@ int check_streamed_unit(const lema_layer& ly, int32_t L, int32_t k, bool final_s
             return set_error(LEMA_ERR_ARG,
                              "unit %d tensor %d: master_out, m_out, v_out must be all NULL or all set",
                              L, j);
-        std::vector<const void*> host = {t.acc};
+        const void* acc[] = {t.acc};
+        LEMA_TRY(check_acc_kind(acc, 1, L, j, kinds, &acc_kind));
+        std::vector<const void*> host;
         if (final_step) {
             host.insert(host.end(), {t.master, t.m, t.v, t.orig_bf16, t.delta, t.w_bf16});
             if (outs) host.insert(host.end(), {t.master_out, t.m_out, t.v_out});
@@ -288,6 +317,7 @@ int check_streamed_unit(const lema_layer& ly, int32_t L, int32_t k, bool final_s
         grad_on_host.back() = (kind == 1);
     }
     (void)k;
+    *acc_on_device = acc_kind == 2;
     if (need > slot_params)
         return set_error(LEMA_ERR_ARG, "unit %d needs %lld slot elements, a slot holds %lld", L,
                          (long long)need, (long long)slot_params);
@@ -313,9 +343,9 @@ int check_streamed_unit(const lema_layer& ly, int32_t L, int32_t k, bool final_s
                 return reinterpret_cast<uintptr_t>(p) ==
                        reinterpret_cast<uintptr_t>(base) + uintptr_t((oj - o_first) * size);
             };
-            // Only the fields this micro-step moves: acc, and at the last micro-step
-            // the optimizer states and outputs as well.
-            bool ok = at(t0.acc, t.acc, 4);
+            // Only the fields this micro-step moves: acc (unless it stays in device
+            // memory), and at the last micro-step the optimizer states and outputs.
+            bool ok = *acc_on_device || at(t0.acc, t.acc, 4);
             if (final_step) {
                 ok = ok && at(t0.master, t.master, 4) && at(t0.m, t.m, 4) && at(t0.v, t.v, 4) &&
                      at(t0.delta, t.delta, 4) && at(t0.orig_bf16, t.orig_bf16, 2) &&
@@ -520,9 +550,13 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
     const bool final_step = micro_step == K;
     // Validate every unit before anything is enqueued.
     std::vector<std::vector<char>> grad_on_host(static_cast<size_t>(n_layers));
-    for (int32_t L = 0; L < n_layers; ++L)
+    std::vector<char> acc_dev(static_cast<size_t>(n_layers), 0);
+    for (int32_t L = 0; L < n_layers; ++L) {
+        bool on_device = false;
         LEMA_TRY(check_streamed_unit(layers[L], L, micro_step, final_step, pool->slot_params,
-                                     grad_on_host[size_t(L)], pool->kinds));
+                                     grad_on_host[size_t(L)], pool->kinds, &on_device));
+        acc_dev[size_t(L)] = on_device;
+    }
     LEMA_TRY(bound_writers(pool));
 
     LEMA_TRY(begin_call(pool, n_layers, caller));
@@ -536,6 +570,33 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
     std::vector<size_t> waits;
     for (int32_t L = 0; L < n_layers; ++L) {
         const lema_layer& ly = layers[L];
+        // Accumulators in device memory stay there: read and written in place by the
+        // kernels, never copied (only the host-resident ones cross the link).
+        const bool dev_acc = acc_dev[size_t(L)] != 0;
+        const bool acc_h2d = acc_in && !dev_acc;
+        if (!final_step && dev_acc && !hooks &&
+            std::none_of(grad_on_host[size_t(L)].begin(), grad_on_host[size_t(L)].end(),
+                         [](char c) { return c != 0; })) {
+            // Nothing of this micro-step crosses the link: the accumulate runs in place
+            // on the compute stream without a slot, so a later call's loads into the
+            // slots need not wait for it (its states stream in meanwhile).
+            int tr = -1;
+            LEMA_TRY(trace_open(pool, pool->cmp, LEMA_STAGE_COMPUTE, L, &tr));
+            ad.clear();
+            for (int32_t j = 0; j < ly.count; ++j) {
+                const lema_tensor& t = ly.tensors[j];
+                if (t.n == 0) continue;
+                AccDesc a;
+                a.acc_in = acc_in ? t.acc : nullptr;
+                a.acc_out = t.acc;
+                a.grad = ly.grads[j];
+                a.n = t.n;
+                ad.push_back(a);
+            }
+            if (!pool->copies_only) LEMA_TRY(run_accum(ad.data(), int32_t(ad.size()), pool->cmp));
+            LEMA_TRY(trace_close(pool, pool->cmp, tr));
+            continue;
+        }
         Slot& sl = pool->slots[size_t(pool->next_slot % pool->n_slots)];
         pool->next_slot++;
         off.assign(size_t(ly.count), 0);
@@ -578,7 +639,7 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
         waits.clear();
         for (int32_t j = 0; j < ly.count; ++j) {
             const lema_tensor& t = ly.tensors[j];
-            const void* reads[] = {acc_in ? t.acc : nullptr, final_step ? t.master : nullptr,
+            const void* reads[] = {acc_h2d ? t.acc : nullptr, final_step ? t.master : nullptr,
                                    final_step ? t.m : nullptr, final_step ? t.v : nullptr};
             for (const void* p : reads) note_writer(pool, p, waits);
         }
@@ -596,7 +657,7 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
                 int64_t o = 0, h = 0, n = 0;
                 field_copy(j, q, &o, &h, &n);
                 if (n == 0) continue;
-                if (acc_in) LEMA_TRY(copy_async(sl.acc + o, t.acc + h, 4 * n, H2D, pool->h2d));
+                if (acc_h2d) LEMA_TRY(copy_async(sl.acc + o, t.acc + h, 4 * n, H2D, pool->h2d));
                 if (final_step) {
                     LEMA_TRY(copy_async(sl.master + o, t.master + h, 4 * n, H2D, pool->h2d));
                     LEMA_TRY(copy_async(sl.m + o, t.m + h, 4 * n, H2D, pool->h2d));
@@ -625,10 +686,11 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
                 const int64_t o = off[size_t(j)] + lo;
                 const uint16_t* g = grad_on_host[size_t(L)][size_t(j)] ? sl.grad + o
                                                                         : ly.grads[j] + lo;
+                float* acc = !acc_in ? nullptr : dev_acc ? ly.tensors[j].acc + lo : sl.acc + o;
                 if (!final_step) {
                     AccDesc a;
-                    a.acc_in = acc_in ? sl.acc + o : nullptr;
-                    a.acc_out = sl.delta + o;
+                    a.acc_in = acc;
+                    a.acc_out = dev_acc ? ly.tensors[j].acc + lo : sl.delta + o;
                     a.grad = g;
                     a.n = hi - lo;
                     ad.push_back(a);
@@ -637,7 +699,7 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
                     x.master_in = sl.master + o;
                     x.m_in = sl.m + o;
                     x.v_in = sl.v + o;
-                    x.acc = acc_in ? sl.acc + o : nullptr;
+                    x.acc = acc;
                     x.orig = sl.orig + o;
                     x.master_out = sl.master_o + o;
                     x.m_out = sl.m_o + o;
@@ -667,7 +729,7 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
             const lema_tensor& t = ly.tensors[j];
             if (t.n == 0) continue;
             if (!final_step) {
-                pool->last_writer[t.acc] = size_t(L);
+                if (!dev_acc) pool->last_writer[t.acc] = size_t(L);
             } else {
                 pool->last_writer[t.master_out ? t.master_out : t.master] = size_t(L);
                 pool->last_writer[t.m_out ? t.m_out : t.m] = size_t(L);
@@ -687,7 +749,8 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
                 float* m_o = t.m_out ? t.m_out : t.m;
                 float* v_o = t.v_out ? t.v_out : t.v;
                 if (!final_step) {
-                    LEMA_TRY(copy_async(t.acc + h, sl.delta + o, 4 * n, D2H, pool->d2h));
+                    if (!dev_acc)
+                        LEMA_TRY(copy_async(t.acc + h, sl.delta + o, 4 * n, D2H, pool->d2h));
                 } else {
                     LEMA_TRY(copy_async(mo + h, sl.master_o + o, 4 * n, D2H, pool->d2h));
                     LEMA_TRY(copy_async(m_o + h, sl.m_o + o, 4 * n, D2H, pool->d2h));
@@ -885,8 +948,9 @@ int64_t carved_q8_bytes(int64_t P) {
 
 int check_streamed_unit_q8(const lema_layer_q8& ly, int32_t L, bool final_step,
                            int64_t slot_params, std::vector<char>& grad_on_host,
-                           std::unordered_map<const void*, int>& kinds) {
+                           std::unordered_map<const void*, int>& kinds, bool* acc_on_device) {
     int64_t need = 0;
+    int acc_kind = 0;
     for (int32_t j = 0; j < ly.count; ++j) {
         const lema_tensor_q8& t = ly.tensors[j];
         if (t.n < 0) return set_error(LEMA_ERR_ARG, "unit %d tensor %d: n must be >= 0", L, j);
@@ -900,7 +964,9 @@ int check_streamed_unit_q8(const lema_layer_q8& ly, int32_t L, bool final_step,
             return set_error(LEMA_ERR_ARG,
                              "unit %d tensor %d: the five *_out fields must be all NULL or all set",
                              L, j);
-        std::vector<const void*> host = {t.acc_q, t.acc_scale};
+        const void* acc[] = {t.acc_q, t.acc_scale};
+        LEMA_TRY(check_acc_kind(acc, 2, L, j, kinds, &acc_kind));
+        std::vector<const void*> host;
         if (final_step) {
             host.insert(host.end(), {t.master, t.m_q, t.m_scale, t.r_q, t.r_scale, t.orig_bf16,
                                      t.delta, t.w_bf16});
@@ -927,6 +993,7 @@ int check_streamed_unit_q8(const lema_layer_q8& ly, int32_t L, bool final_step,
                              "unit %d tensor %d: grad must be device or pinned host memory", L, j);
         grad_on_host.back() = (kind == 1);
     }
+    *acc_on_device = acc_kind == 2;
     if (need > slot_params)
         return set_error(LEMA_ERR_ARG, "unit %d needs %lld slot elements, a slot holds %lld", L,
                          (long long)need, (long long)slot_params);
@@ -949,7 +1016,8 @@ int check_streamed_unit_q8(const lema_layer_q8& ly, int32_t L, bool final_step,
             auto at = [](const void* base, const void* p, int64_t bytes) {
                 return reinterpret_cast<uintptr_t>(p) == reinterpret_cast<uintptr_t>(base) + uintptr_t(bytes);
             };
-            bool ok = at(t0.acc_q, t.acc_q, de) && at(t0.acc_scale, t.acc_scale, 4 * db);
+            bool ok = *acc_on_device ||
+                      (at(t0.acc_q, t.acc_q, de) && at(t0.acc_scale, t.acc_scale, 4 * db));
             if (final_step) {
                 ok = ok && at(t0.master, t.master, 4 * de) && at(t0.m_q, t.m_q, de) &&
                      at(t0.m_scale, t.m_scale, 4 * db) && at(t0.r_q, t.r_q, de) &&
@@ -1014,9 +1082,13 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
     const bool final_step = micro_step == K;
     const bool acc_in = micro_step >= 2;
     std::vector<std::vector<char>> grad_on_host(static_cast<size_t>(n_layers));
-    for (int32_t L = 0; L < n_layers; ++L)
+    std::vector<char> acc_dev(static_cast<size_t>(n_layers), 0);
+    for (int32_t L = 0; L < n_layers; ++L) {
+        bool on_device = false;
         LEMA_TRY(check_streamed_unit_q8(layers[L], L, final_step, pool->slot_params,
-                                        grad_on_host[size_t(L)], pool->kinds));
+                                        grad_on_host[size_t(L)], pool->kinds, &on_device));
+        acc_dev[size_t(L)] = on_device;
+    }
     LEMA_TRY(bound_writers(pool));
     LEMA_TRY(begin_call(pool, n_layers, caller));
 
@@ -1029,6 +1101,32 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
     auto blocks = [](int64_t n) { return (n + kQBlock - 1) / kQBlock; };
     for (int32_t L = 0; L < n_layers; ++L) {
         const lema_layer_q8& ly = layers[L];
+        const bool dev_acc = acc_dev[size_t(L)] != 0;   // as in lema_stream_layers
+        const bool acc_h2d = acc_in && !dev_acc;
+        if (!final_step && dev_acc && !hooks &&
+            std::none_of(grad_on_host[size_t(L)].begin(), grad_on_host[size_t(L)].end(),
+                         [](char c) { return c != 0; })) {
+            // an accumulate that moves nothing: in place, no slot (lema_stream_layers)
+            int tr = -1;
+            LEMA_TRY(trace_open(pool, pool->cmp, LEMA_STAGE_COMPUTE, L, &tr));
+            ad.clear();
+            for (int32_t j = 0; j < ly.count; ++j) {
+                const lema_tensor_q8& t = ly.tensors[j];
+                if (t.n == 0) continue;
+                AccDescQ8 a;
+                a.acc_q_in = acc_in ? t.acc_q : nullptr;
+                a.acc_scale_in = acc_in ? t.acc_scale : nullptr;
+                a.acc_q_out = t.acc_q;
+                a.acc_scale_out = t.acc_scale;
+                a.grad = ly.grads[j];
+                a.n = t.n;
+                ad.push_back(a);
+            }
+            if (!pool->copies_only)
+                LEMA_TRY(run_accum_q8(ad.data(), int32_t(ad.size()), pool->cmp));
+            LEMA_TRY(trace_close(pool, pool->cmp, tr));
+            continue;
+        }
         Slot& sl0 = pool->slots[size_t(pool->next_slot % pool->n_slots)];
         pool->next_slot++;
         const SlotQ8 sl = carve_q8(sl0, pool->slot_params);
@@ -1079,7 +1177,7 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
         waits.clear();
         for (int32_t j = 0; j < ly.count; ++j) {
             const lema_tensor_q8& t = ly.tensors[j];
-            const void* reads[] = {acc_in ? t.acc_q : nullptr, final_step ? t.master : nullptr,
+            const void* reads[] = {acc_h2d ? t.acc_q : nullptr, final_step ? t.master : nullptr,
                                    final_step ? t.m_q : nullptr, final_step ? t.r_q : nullptr};
             for (const void* p : reads) note_writer(pool, p, waits);
         }
@@ -1098,7 +1196,7 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
                 field_copy(j, q, &o, &h, &n, &nb);
                 if (n == 0) continue;
                 const int64_t b = o / kQBlock, hb = h / kQBlock;
-                if (acc_in) {
+                if (acc_h2d) {
                     LEMA_TRY(copy_async(sl.acc_q + o, t.acc_q + h, n, H2D, pool->h2d));
                     LEMA_TRY(copy_async(sl.acc_s + b, t.acc_scale + hb, 4 * nb, H2D, pool->h2d));
                 }
@@ -1130,12 +1228,18 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
                 const int64_t o = off[size_t(j)] + lo, b = o / kQBlock;
                 const uint16_t* g = grad_on_host[size_t(L)][size_t(j)] ? sl.grad + o
                                                                         : ly.grads[j] + lo;
+                // a device-resident accumulator: tensor j's own codes and scales
+                // (lo is a whole number of blocks: slice bounds are whole chunks)
+                const lema_tensor_q8& t = ly.tensors[j];
+                int8_t* acc_q = !acc_in ? nullptr : dev_acc ? t.acc_q + lo : sl.acc_q + o;
+                float* acc_s = !acc_in ? nullptr : dev_acc ? t.acc_scale + lo / kQBlock
+                                                           : sl.acc_s + b;
                 if (!final_step) {
                     AccDescQ8 a;
-                    a.acc_q_in = acc_in ? sl.acc_q + o : nullptr;
-                    a.acc_scale_in = acc_in ? sl.acc_s + b : nullptr;
-                    a.acc_q_out = sl.acc_q_o + o;
-                    a.acc_scale_out = sl.acc_s_o + b;
+                    a.acc_q_in = acc_q;
+                    a.acc_scale_in = acc_s;
+                    a.acc_q_out = dev_acc ? t.acc_q + lo : sl.acc_q_o + o;
+                    a.acc_scale_out = dev_acc ? t.acc_scale + lo / kQBlock : sl.acc_s_o + b;
                     a.grad = g;
                     a.n = hi - lo;
                     ad.push_back(a);
@@ -1146,8 +1250,8 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
                     x.m_scale_in = sl.m_s + b;
                     x.r_q_in = sl.r_q + o;
                     x.r_scale_in = sl.r_s + b;
-                    x.acc_q = acc_in ? sl.acc_q + o : nullptr;
-                    x.acc_scale = acc_in ? sl.acc_s + b : nullptr;
+                    x.acc_q = acc_q;
+                    x.acc_scale = acc_s;
                     x.grad = g;
                     x.orig = sl.orig + o;
                     x.master_out = sl.master_o + o;
@@ -1180,7 +1284,7 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
             const lema_tensor_q8& t = ly.tensors[j];
             if (t.n == 0) continue;
             if (!final_step) {
-                pool->last_writer[t.acc_q] = size_t(L);
+                if (!dev_acc) pool->last_writer[t.acc_q] = size_t(L);
             } else {
                 pool->last_writer[t.master_out ? t.master_out : t.master] = size_t(L);
                 pool->last_writer[t.m_q_out ? t.m_q_out : t.m_q] = size_t(L);
@@ -1203,8 +1307,11 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
                 uint8_t* rq = t.r_q_out ? t.r_q_out : t.r_q;
                 float* rs = t.r_scale_out ? t.r_scale_out : t.r_scale;
                 if (!final_step) {
-                    LEMA_TRY(copy_async(t.acc_q + h, sl.acc_q_o + o, n, D2H, pool->d2h));
-                    LEMA_TRY(copy_async(t.acc_scale + hb, sl.acc_s_o + b, 4 * nb, D2H, pool->d2h));
+                    if (!dev_acc) {
+                        LEMA_TRY(copy_async(t.acc_q + h, sl.acc_q_o + o, n, D2H, pool->d2h));
+                        LEMA_TRY(copy_async(t.acc_scale + hb, sl.acc_s_o + b, 4 * nb, D2H,
+                                            pool->d2h));
+                    }
                 } else {
                     LEMA_TRY(copy_async(mo + h, sl.master_o + o, 4 * n, D2H, pool->d2h));
                     LEMA_TRY(copy_async(mq + h, sl.m_q_o + o, n, D2H, pool->d2h));

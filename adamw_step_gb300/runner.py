@@ -127,13 +127,18 @@ class ResidentRunner:
 class StreamedRunner:
     """States in pinned host RAM, streamed unit by unit through a slot pool."""
 
-    def __init__(self, cfg, grads: DeviceGrads, w0_list=None, n_slots=None, packed=True):
+    def __init__(self, cfg, grads: DeviceGrads, w0_list=None, n_slots=None, packed=True,
+                 acc_on_device=False):
         """packed: lay each unit's host states out like a slot (one copy per field
-        per unit); False: an independent buffer per tensor (one copy per tensor)."""
+        per unit); False: an independent buffer per tensor (one copy per tensor).
+        acc_on_device: the accumulators live in HBM (only the optimizer states and
+        weights stream)."""
         self.cfg = cfg
         self.grads = grads
+        self.acc_on_device = acc_on_device
         units = [cfg.unit_tensors(u) for u in range(cfg.n_units)]
-        self.state = HostState(w0_list or initial_weights(cfg), units=units if packed else None)
+        self.state = HostState(w0_list or initial_weights(cfg), units=units if packed else None,
+                               acc_device="cuda" if acc_on_device else None)
         self.pool = Pool(n_slots or cfg.n_slots, slot_params_for(cfg))
         self.layers = Layers(self.state, [cfg.unit_tensors(u) for u in range(cfg.n_units)])
         self.hp = hparams(cfg.hyper, cfg.accum_steps)
@@ -156,8 +161,9 @@ class StreamedRunner:
     def link_bytes_per_step(self, host_grads=False):
         """(H2D, D2H) bytes one optimizer step moves over the host link."""
         n, K = self.state.numel, self.cfg.accum_steps
-        h2d = n * (14 + 4 * (K - 1) + (2 * K if host_grads else 0))
-        d2h = n * (18 + 4 * (K - 1))
+        acc = 0 if self.acc_on_device else 4 * (K - 1)
+        h2d = n * (14 + acc + (2 * K if host_grads else 0))
+        d2h = n * (18 + acc)
         return h2d, d2h
 
     def close(self):
@@ -224,12 +230,15 @@ class StreamedRunnerQ8:
     last micro-batch grad is folded into the step and the host accumulator keeps
     micro-steps 1..K-1."""
 
-    def __init__(self, cfg, grads: DeviceGrads, w0_list=None, n_slots=None, packed=True):
+    def __init__(self, cfg, grads: DeviceGrads, w0_list=None, n_slots=None, packed=True,
+                 acc_on_device=False):
         self.cfg = cfg
         self.grads = grads
+        self.acc_on_device = acc_on_device
         units = [cfg.unit_tensors(u) for u in range(cfg.n_units)]
         self.state = HostStateQ8(w0_list or initial_weights(cfg),
-                                 units=units if packed else None)
+                                 units=units if packed else None,
+                                 acc_device="cuda" if acc_on_device else None)
         self.pool = Pool(n_slots or cfg.n_slots, slot_params_for_q8(cfg))
         self.layers = LayersQ8(self.state, units)
         self.hp = hparams(cfg.hyper, cfg.accum_steps)
@@ -255,7 +264,7 @@ class StreamedRunnerQ8:
         K = self.cfg.accum_steps
         n = self.state.numel
         nb = sum((t["orig"].numel() + Q8_BLOCK - 1) // Q8_BLOCK for t in self.state.tensors)
-        acc = n + 4 * nb                                  # codes + scales of the accumulator
+        acc = 0 if self.acc_on_device else n + 4 * nb   # codes + scales of the accumulator
         h2d = 8 * n + 8 * nb + (K - 1) * acc + (2 * K * n if host_grads else 0)
         d2h = 12 * n + 8 * nb + (K - 1) * acc
         return h2d, d2h
@@ -273,13 +282,15 @@ class DiskRunner:
     StreamedRunnerQ8)."""
 
     def __init__(self, cfg, grads: DeviceGrads, path, w0_list=None, n_slots=None,
-                 flags=lema.LEMA_DISK_DIRECT, n_io_threads=8, q8=False):
+                 flags=lema.LEMA_DISK_DIRECT, n_io_threads=8, q8=False, acc_on_device=False):
         self.cfg = cfg
         self.grads = grads
         self.q8 = q8
+        self.acc_on_device = acc_on_device
         units = [cfg.unit_tensors(u) for u in range(cfg.n_units)]
         State = DiskStateQ8 if q8 else DiskState
-        self.state = State(path, w0_list or initial_weights(cfg), units, flags, n_io_threads)
+        self.state = State(path, w0_list or initial_weights(cfg), units, flags, n_io_threads,
+                           acc_device="cuda" if acc_on_device else None)
         self.pool = Pool(n_slots or cfg.n_slots,
                          slot_params_for_q8(cfg) if q8 else slot_params_for(cfg))
         self.layers = DiskLayersQ8(self.state) if q8 else DiskLayers(self.state)
@@ -318,9 +329,10 @@ class DiskRunner:
         n, K = self.state.numel, self.cfg.accum_steps
         if self.q8:
             nb = sum((x + Q8_BLOCK - 1) // Q8_BLOCK for x in self.state.sizes)
-            acc = n + 4 * nb
+            acc = 0 if self.acc_on_device else n + 4 * nb
             return 8 * n + 8 * nb + (K - 1) * acc, 12 * n + 8 * nb + (K - 1) * acc
-        return n * (14 + 4 * (K - 1)), n * (18 + 4 * (K - 1))
+        acc = 0 if self.acc_on_device else 4 * (K - 1)
+        return n * (14 + acc), n * (18 + acc)
 
     def close(self):
         self.pool.close()

@@ -28,25 +28,30 @@ def _ptr(t: torch.Tensor | None) -> int | None:
 class _State:
     fields_f32 = ("master", "m", "v", "acc", "delta")
 
-    def __init__(self, w0_list, device, pin: bool, units=None):
+    def __init__(self, w0_list, device, pin: bool, units=None, acc_device=None):
         """units (pinned host only): lists of tensor indices.  Each unit's fields are
         then laid out like a VRAM slot -- one block per field, tensor j at the
         64-element-aligned offset the slot uses -- so the pool moves each field of
-        a unit with one copy (LEMA_UNIT_PACKED)."""
+        a unit with one copy (LEMA_UNIT_PACKED).  acc_device (pinned host only): keep
+        the accumulators in that device's memory instead (same layout), where the
+        pool updates them in place and never copies them."""
         self.tensors = [None] * len(w0_list)
         self.pinned = None
         self.units = [list(u) for u in units] if (pin and units is not None) else None
         if pin:
             groups = self.units or [[j] for j in range(len(w0_list))]
             sizes = []
+            host_f32 = [f for f in self.fields_f32 if not (acc_device and f == "acc")]
             for u in groups:
                 P = sum(_pad(w0_list[j].numel()) for j in u)
-                sizes += [(P, torch.bfloat16)] * 2 + [(P, torch.float32)] * 5
+                sizes += [(P, torch.bfloat16)] * 2 + [(P, torch.float32)] * len(host_f32)
             # one registered arena for every buffer of every tensor
             self.pinned = PinnedBuffers(PinnedBuffers.arena_size(sizes))
             for u in groups:
                 P = sum(_pad(w0_list[j].numel()) for j in u)
-                block = {f: self.pinned.zeros(P, torch.float32) for f in self.fields_f32}
+                block = {f: self.pinned.zeros(P, torch.float32) for f in host_f32}
+                if acc_device:
+                    block["acc"] = torch.zeros(P, dtype=torch.float32, device=acc_device)
                 block["orig"] = self.pinned.zeros(P, torch.bfloat16)
                 block["w"] = self.pinned.zeros(P, torch.bfloat16)
                 o = 0
@@ -130,10 +135,10 @@ class DeviceState(_State):
 
 class HostState(_State):
     """All states in pinned host RAM (the streamed residency); `units` packs each
-    unit like a slot."""
+    unit like a slot; acc_device keeps the accumulators in device memory."""
 
-    def __init__(self, w0_list, units=None):
-        super().__init__(w0_list, "cpu", pin=True, units=units)
+    def __init__(self, w0_list, units=None, acc_device=None):
+        super().__init__(w0_list, "cpu", pin=True, units=units, acc_device=acc_device)
 
 
 def hparams(hyper, accum_steps: int) -> LemaHparams:
@@ -281,20 +286,24 @@ class DeviceStateQ8:
 class HostStateQ8(DeviceStateQ8):
     """8-bit states in pinned host RAM (the streamed residency).  With `units`, each
     unit's fields are laid out like an 8-bit slot: one block per field, tensor j at
-    its 1024-element offset o_j and its scales at o_j / 256 (LEMA_UNIT_PACKED)."""
+    its 1024-element offset o_j and its scales at o_j / 256 (LEMA_UNIT_PACKED).
+    acc_device: the accumulator's codes and scales in that device's memory instead
+    (same layout)."""
 
-    def __init__(self, w0_list, units=None):
+    def __init__(self, w0_list, units=None, acc_device=None):
         self.units = [list(u) for u in units] if units is not None else None
         groups = self.units or [[j] for j in range(len(w0_list))]
+        on_device = ("acc_q", "acc_scale") if acc_device else ()
         sizes = []
         for u in groups:
             P = sum(_pad_q8(w0_list[j].numel()) for j in u)
-            sizes += [(P // per, dt) for _, dt, per in _Q8_FIELDS]
+            sizes += [(P // per, dt) for f, dt, per in _Q8_FIELDS if f not in on_device]
         self.pinned = PinnedBuffers(PinnedBuffers.arena_size(sizes))
         self.tensors = [None] * len(w0_list)
         for u in groups:
             P = sum(_pad_q8(w0_list[j].numel()) for j in u)
-            block = {f: self.pinned.zeros(P // per, dt) for f, dt, per in _Q8_FIELDS}
+            block = {f: (torch.zeros(P // per, dtype=dt, device=acc_device) if f in on_device
+                         else self.pinned.zeros(P // per, dt)) for f, dt, per in _Q8_FIELDS}
             o = 0
             for j in u:
                 n = w0_list[j].numel()
@@ -369,7 +378,10 @@ class DiskState:
     def _block_bytes(self, Q: int) -> int:
         return 20 * Q
 
-    def __init__(self, path, w0_list, units, flags=lema.LEMA_DISK_DIRECT, n_io_threads=8):
+    def __init__(self, path, w0_list, units, flags=lema.LEMA_DISK_DIRECT, n_io_threads=8,
+                 acc_device=None):
+        """acc_device: keep the accumulators in that device's memory (same layout)
+        instead of pinned host RAM."""
         import numpy as np
         self.path = path
         self.units = [list(u) for u in units]
@@ -407,12 +419,17 @@ class DiskState:
             # on disk before the library reads it with O_DIRECT (past the page cache)
             f.flush()
             os.fsync(f.fileno())
-        self.pinned = PinnedBuffers(PinnedBuffers.arena_size(
-            [(p // per, dt) for p in P for dt, per in self._ACC.values()]))
+        if acc_device:
+            self.pinned = None
+            alloc = lambda n, dt: torch.zeros(n, dtype=dt, device=acc_device)  # noqa: E731
+        else:
+            self.pinned = PinnedBuffers(PinnedBuffers.arena_size(
+                [(p // per, dt) for p in P for dt, per in self._ACC.values()]))
+            alloc = self.pinned.zeros
         self.acc = {f: [None] * len(w0_list) for f in self._ACC}
         for ui, u in enumerate(self.units):
             for f, (dt, per) in self._ACC.items():
-                block = self.pinned.zeros(P[ui] // per, dt)
+                block = alloc(P[ui] // per, dt)
                 for j in u:
                     o = self.offset_in_unit[j] // per
                     self.acc[f][j] = block[o:o + (self.sizes[j] + per - 1) // per]
@@ -434,8 +451,8 @@ class DiskState:
         """(master, m, v, acc, delta, orig_u16, w_u16) of tensor j, read from the file
         (after sync())."""
         f = {name: self._read_np(j, name) for name in self._FIELDS}
-        return [f["master"], f["m"], f["v"], self.acc["acc"][j].numpy().copy(), f["delta"],
-                f["orig"], f["w"]]
+        return [f["master"], f["m"], f["v"], self.acc["acc"][j].cpu().numpy().copy(),
+                f["delta"], f["orig"], f["w"]]
 
     def _place(self, j, f):
         """(byte offset in the file, value count, torch dtype) of field f of tensor j."""
@@ -532,7 +549,7 @@ class DiskStateQ8(DiskState):
         fields read from the file (after sync())."""
         out = {f: self._read_np(j, f) for f in self._FIELDS}
         for f in self._ACC:
-            out[f] = self.acc[f][j].numpy().copy()
+            out[f] = self.acc[f][j].cpu().numpy().copy()
         return out
 
 

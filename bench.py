@@ -91,6 +91,9 @@ def parse():
     p.add_argument("--no-hidden", action="store_true",
                    help="streamed legs: skip the copies-only steps that show whether the "
                         "compute is hidden behind the copies")
+    p.add_argument("--acc-on-device", action="store_true",
+                   help="streamed legs and the disk tier: keep the gradient accumulators in "
+                        "HBM (only the optimizer states and weights cross the host link)")
     p.add_argument("--no-whole-model", action="store_true",
                    help="default run: skip the whole-model streamed leg (TinyLlama-1.1B "
                         "shape, states in pinned host RAM)")
@@ -398,8 +401,10 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
     from adamw_step_gb300.runner import DeviceGrads, StreamedRunner, StreamedRunnerQ8
     q8 = getattr(args, "q8", False)
     peaks = host_link_peaks(1 << 30, 3)
+    acc_dev = getattr(args, "acc_on_device", False)
     sr = (StreamedRunnerQ8 if q8 else StreamedRunner)(cfg, DeviceGrads(cfg, pin_host=host_grads),
-                                                      n_slots=getattr(args, "slots", 0) or None)
+                                                      n_slots=getattr(args, "slots", 0) or None,
+                                                      acc_on_device=acc_dev)
     if getattr(args, "slices", 0):
         sr.pool.slices(args.slices, args.min_slice)
     huge = anon_huge_bytes()
@@ -450,7 +455,8 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
            "path": f"lema_stream_layers{'_q8' if q8 else ''}, "
                    f"{getattr(args, 'slots', 0) or cfg.n_slots} VRAM slots, "
                    f"3 streams, {'8-bit' if q8 else 'fp32'} states "
-                   f"{'and bf16 grads ' if host_grads else ''}in pinned host RAM"}
+                   f"{'and bf16 grads ' if host_grads else ''}in pinned host RAM"
+                   f"{', accumulators resident in HBM' if acc_dev else ''}"}
     sr.close()
     del sr
     torch.cuda.empty_cache()
@@ -593,7 +599,8 @@ def disk_leg(cfg, args, world, stream, steps, warmup=1):
                                  lema.LEMA_DISK_DIRECT, 8)
     path = os.path.join(args.disk, f"lema_states_{tag}.bin")
     q8 = getattr(args, "q8", False)
-    r = DiskRunner(cfg, DeviceGrads(cfg), path, q8=q8)
+    acc_dev = getattr(args, "acc_on_device", False)
+    r = DiskRunner(cfg, DeviceGrads(cfg), path, q8=q8, acc_on_device=acc_dev)
     try:
         for t in range(warmup):
             r.step(t, stream)
@@ -624,7 +631,7 @@ def disk_leg(cfg, args, world, stream, steps, warmup=1):
             "disk_peaks_gbs": {k: round(v, 2) for k, v in peaks.items()},
             "path": f"lema_stream_layers_disk{'_q8' if q8 else ''}: states in one file "
                     f"(O_DIRECT, 8 IO threads), 3 pinned staging buffers, {cfg.n_slots} VRAM "
-                    f"slots, 3 streams"}
+                    f"slots, 3 streams, accumulators in {'HBM' if acc_dev else 'pinned RAM'}"}
 
 
 def streamed_main(cfg, args, rank, world):
@@ -653,13 +660,16 @@ def streamed_main(cfg, args, rank, world):
                 "dtype": "f32", "data": "synthetic",
                 "config": dict(config_block(cfg, args, world, l2="bound by the disk; "
                                             "no L2 reuse across units"),
-                               residency="disk file + pinned-RAM accumulators, streamed"),
+                               residency="disk file + " + ("HBM" if args.acc_on_device
+                                                           else "pinned-RAM")
+                               + " accumulators, streamed"),
                 "roofline": roof, "disk": leg, "clocks": clk, "cpu_baseline": None,
                 "gpu_launches": args.steps * sum(
                     cfg.accum_steps * launches_per_call(len(cfg.unit_tensors(u)), args.q8)
                     for u in range(cfg.n_units))}), flush=True)
         return
-    # pinned states (24 B/param fp32, about 15 with 8-bit moments) + probes + runtime
+    # pinned states (24 B/param fp32, about 15 with 8-bit moments; an upper bound with
+    # the accumulators in HBM) + probes + runtime
     need = cfg.params * (16 if args.q8 else 24) + (8 << 30)
     if mem_available_bytes() < need:
         print(json.dumps({"metric": METRIC, "error": f"needs {need / 2 ** 30:.0f} GiB of host "
@@ -688,7 +698,9 @@ def streamed_main(cfg, args, rank, world):
                 "dtype": "f32", "data": "synthetic",
                 "config": dict(config_block(cfg, args, world, l2="bound by the host link; "
                                             "no L2 reuse across units"),
-                               residency="pinned host, streamed"),
+                               residency="pinned host, streamed" + (
+                                   "; accumulators resident in HBM" if args.acc_on_device
+                                   else "")),
                 "roofline": roof, "streamed": leg, "clocks": clk, "cpu_baseline": cpu,
                 "gpu_launches": args.steps * sum(
                     cfg.accum_steps * launches_per_call(len(cfg.unit_tensors(u)), args.q8)

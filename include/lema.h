@@ -301,7 +301,8 @@ typedef struct lema_adamw_hparams {
  *            tensor's pointer plus o_j - o_first elements, o_j = sum over i < j of
  *            n_i rounded up to a multiple of 64,
  *            and the gaps between tensors belong to the caller's same allocation
- *            (tensors with n == 0 are skipped: they carry no data).
+ *            (tensors with n == 0 are skipped: they carry no data).  Accumulators
+ *            kept in device memory (below) are exempt from the rule.
  *            The pool then moves each field of the unit with one copy (gaps
  *            included) instead of one per tensor.  Checked: a unit flagged packed
  *            whose pointers do not follow the rule is rejected (LEMA_ERR_ARG). */
@@ -340,6 +341,20 @@ int lema_pool_create(int32_t n_slots, int64_t slot_params, lema_pool** out);
  *                   partial sums: after k == K it still holds the sum of micro-steps
  *                   1..K-1 (never written when K == 1), and the next step's k == 1
  *                   starts again from +0.0 without reading it.
+ * Accumulator residency (page "LEMA: Layer-wise Efficient Memory Abstraction",
+ * section "TensorStore: Unified Streaming Core": weights, optimizer states and
+ * gradient accumulators each with a residency policy of their own): a unit's acc
+ * may instead be device memory (16-byte aligned, all of the unit's non-empty
+ * tensors alike; a unit mixing the two is rejected with LEMA_ERR_ARG).  It then
+ * stays in HBM: the compute stage reads and updates it in place (k < K) or reads it
+ * (k == K), and no acc copy crosses the host link, which leaves master, m, v, orig
+ * in and master', m', v', delta, w_bf16 out at k == K, and nothing but host grads
+ * at k < K.  A unit whose grads are device memory as well moves nothing at k < K
+ * and takes no slot: its accumulate runs on the compute stream in call order, and
+ * the copies of the next calls (the states the step at k == K loads) need not wait
+ * for it.  Its contents follow the same rule as the host acc (after k == K the sum
+ * of micro-steps 1..K-1).  It is written on the pool's compute stream: order the
+ * caller's own accesses with lema_pool_wait_stream or lema_pool_sync.
  * With two or more slots the three stages of consecutive units overlap: while unit
  * L is computed, unit L+1 is copied in and unit L-1 copied out; a packed unit also
  * moves in slices (lema_pool_slices), so its own three stages overlap too.  Results
@@ -377,6 +392,9 @@ typedef struct lema_layer_q8 {
  * moves master, m and sqrt(v) codes + scales and orig in, runs the 8-bit step with
  * the last grad folded in, and moves master, the codes + scales, delta and w_bf16
  * out (the host accumulator keeps micro-steps 1..K-1, as in lema_stream_layers).
+ * As there, a unit's accumulators (acc_q and acc_scale of all its non-empty
+ * tensors) may be device memory instead: they then stay in HBM and are updated in
+ * place, and no accumulator copy crosses the host link.
  * Results equal lema_accum_grad_q8 + lema_adamw_step_q8 (last grad folded in) on
  * the same values, bit for bit.  Each unit must fit a slot with its tensors at
  * 1024-element offsets.  Errors as lema_stream_layers. */
@@ -393,8 +411,8 @@ int lema_stream_layers_q8(lema_pool* pool, const lema_layer_q8* layers, int32_t 
  * Fine-Tuning" (host memory holds the optimizer state and the accumulated grads,
  * a file can back them).  Reading taken here: the optimizer
  * states (master, m, v), the original and working weights and the delta live in
- * one file; the gradient accumulators stay in pinned RAM, since every micro-step
- * rewrites them.  The step's last micro-step streams each unit file -> pinned
+ * one file; the gradient accumulators stay in pinned RAM (or device memory, as
+ * lema_stream_layers allows), since every micro-step rewrites them.  The step's last micro-step streams each unit file -> pinned
  * staging buffer -> VRAM slot -> staging -> file; three staging buffers rotate so
  * that the read of unit L+2, the GPU work of unit L and the write-back of unit L-1
  * run at once.  File IO runs on the library's own threads (pread/pwrite, O_DIRECT
@@ -464,7 +482,7 @@ int lema_disk_close(lema_disk* disk);
 /* lema_stream_layers (LEMA_STREAMED) with the states of unit L in the disk's unit L
  * (L < the disk's n_units; each layer's packed size must equal its P_L).  In the
  * layers only n, acc (pinned host, at the slot offsets when the layer is flagged
- * LEMA_UNIT_PACKED) and the grads are read; the other pointers of each tensor
+ * LEMA_UNIT_PACKED; or device memory, as in lema_stream_layers) and the grads are read; the other pointers of each tensor
  * must be NULL.  Micro-steps k < K touch no file (the accumulator streams as in
  * lema_stream_layers).  At k == K the call blocks on the host until the last
  * unit's read has finished and its GPU work is enqueued, and queues every unit's
@@ -477,7 +495,7 @@ int lema_stream_layers_disk(lema_pool* pool, lema_disk* disk, const lema_layer* 
 
 /* lema_stream_layers_disk for a disk opened with LEMA_DISK_Q8: lema_stream_layers_q8
  * with the states of unit L in the disk's unit L.  In the layers only n, acc_q and
- * acc_scale (pinned host) and the grads are read; the other pointers must be NULL.
+ * acc_scale (pinned host or device memory) and the grads are read; the other pointers must be NULL.
  * Results equal lema_stream_layers_q8's on the same values, bit for bit.  Errors as
  * lema_stream_layers_disk (LEMA_ERR_ARG when the disk's kind and the call differ). */
 int lema_stream_layers_disk_q8(lema_pool* pool, lema_disk* disk, const lema_layer_q8* layers,

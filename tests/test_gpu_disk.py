@@ -48,6 +48,32 @@ def test_disk_tier_matches_oracle(tmp_path, K, flags):
         r.close()
 
 
+@pytest.mark.parametrize("q8", [False, True], ids=["fp32", "8-bit"])
+def test_disk_tier_device_accumulators(tmp_path, q8):
+    """The disk tier with its accumulators in HBM instead of pinned RAM: the file
+    and the accumulators equal the oracle's."""
+    from oracle.runner import run_config_q8
+    from test_gpu_stream_q8 import compare
+    sizes, units = (Q8_SIZES, Q8_UNITS) if q8 else (RAGGED, [i // 3 for i in range(len(RAGGED))])
+    cfg = small_config(sizes, K=3, steps=2, units=units)
+    r = DiskRunner(cfg, DeviceGrads(cfg), str(tmp_path / "acc_dev.bin"), q8=q8,
+                   acc_on_device=True)
+    for t in range(cfg.steps):
+        r.step(t)
+    r.sync()
+    try:
+        if q8:
+            compare(r.state, run_config_q8(cfg, fused=True), "q8 disk, device acc")
+        else:
+            ref = oracle_states(cfg)
+            for j in ref:
+                want = dict(oracle_dict(ref[j]), acc=last_step_acc(cfg, j))
+                rep = check_tensor(state_dict(r.state, j), want, f"disk device acc tensor {j}")
+                assert sum(rep.values()) == 0, rep
+    finally:
+        r.close()
+
+
 def test_disk_tier_equals_streamed_bits(tmp_path):
     """Nine units of one to three tensors, host-resident grads, two IO threads: the
     file and accumulators end bit-identical to the pinned-RAM streamed path's."""

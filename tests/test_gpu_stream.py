@@ -80,6 +80,63 @@ def test_streamed_sliced_units_match_oracle(host_grads):
     sr.close()
 
 
+@pytest.mark.parametrize("K", [1, 2, 3])
+@pytest.mark.parametrize("host_grads,slices,packed", [(False, 1, True), (True, 1, False),
+                                                      (False, 4, True), (True, 4, True)],
+                         ids=["device-grads", "host-grads-per-tensor", "sliced",
+                              "host-grads-sliced"])
+def test_streamed_device_accumulators_match_oracle(K, host_grads, slices, packed):
+    """Accumulators kept in HBM while the optimizer states stream: the same bits as
+    the oracle, the device acc holding micro-steps 1..K-1 of the last step (as the
+    host acc would)."""
+    cfg = small_config(RAGGED, K=K, steps=3, units=ragged_units())
+    sr = StreamedRunner(cfg, DeviceGrads(cfg, pin_host=host_grads), n_slots=2, packed=packed,
+                        acc_on_device=True)
+    assert all(t["acc"].is_cuda for t in sr.state.tensors)
+    sr.pool.slices(slices, 8192)
+    try:
+        for t in range(cfg.steps):
+            sr.step(t)
+        sr.pool.sync(600_000)
+        assert check_streamed(cfg, sr, oracle_states(cfg), label=f"device acc K={K}") == 0
+    finally:
+        sr.close()
+
+
+def test_streamed_device_accumulators_per_unit_and_mixed_unit_rejected():
+    """Units may differ (unit 0's accumulators in HBM, the others' in pinned RAM);
+    a unit that mixes the two is rejected before anything is enqueued."""
+    cfg = small_config(RAGGED, K=3, steps=2, units=ragged_units())
+    sr = StreamedRunner(cfg, DeviceGrads(cfg), n_slots=2)
+    unit0 = cfg.unit_tensors(0)
+    try:
+        # a mixed unit: the first tensor's accumulator alone on the device
+        host_acc = sr.state.tensors[unit0[0]]["acc"]
+        sr.state.tensors[unit0[0]]["acc"] = torch.zeros(host_acc.numel(), device="cuda")
+        mixed = Layers(sr.state, [cfg.unit_tensors(u) for u in range(cfg.n_units)], packed=False)
+        arr, keep = mixed.build([sr.grads(j, 0, 0) for j in range(len(cfg.tensors))])
+        with pytest.raises(lema.LemaError) as e:
+            sr.pool.stream_layers(arr, 1, sr.hp, 1)
+        assert e.value.status == lema.LEMA_ERR_ARG and "must all be pinned host" in e.value.message
+        # the whole of unit 0 on the device, packed like the host block
+        P = sum(-(-sr.state.tensors[j]["acc"].numel() // 64) * 64 for j in unit0)
+        block = torch.zeros(P, device="cuda")
+        o = 0
+        for j in unit0:
+            n = sr.state.tensors[j]["orig"].numel()
+            sr.state.tensors[j]["acc"] = block[o:o + n]
+            o += -(-n // 64) * 64
+        sr.layers = Layers(sr.state, [cfg.unit_tensors(u) for u in range(cfg.n_units)],
+                           packed=False)
+        sr._built.clear()
+        for t in range(cfg.steps):
+            sr.step(t)
+        sr.pool.sync(600_000)
+        assert check_streamed(cfg, sr, oracle_states(cfg), label="unit 0 on the device") == 0
+    finally:
+        sr.close()
+
+
 def test_copies_only_mode_leaves_the_pool_usable():
     """The measurement mode enqueues a streamed step's copies without kernels (its
     host outputs are then slot contents, not results); switched off again, the same
@@ -144,6 +201,19 @@ def test_config3_full():
     sr = run_streamed(cfg)
     assert check_streamed(cfg, sr, oracle_states(cfg), label="config 3") == 0
     sr.close()
+
+
+def test_config3_device_accumulators_full():
+    """Config 3 with its accumulators in HBM: every element against the oracle."""
+    cfg = configs.CONFIGS[3]
+    sr = StreamedRunner(cfg, DeviceGrads(cfg), acc_on_device=True)
+    try:
+        for t in range(cfg.steps):
+            sr.step(t)
+        sr.pool.sync(600_000)
+        assert check_streamed(cfg, sr, oracle_states(cfg), label="config 3, device acc") == 0
+    finally:
+        sr.close()
 
 
 def test_unit_larger_than_slot_is_rejected_before_any_copy():

@@ -77,6 +77,46 @@ def test_q8_streamed_bit_exact(K, packed):
         sr.close()
 
 
+@pytest.mark.parametrize("K", [1, 2, 3])
+@pytest.mark.parametrize("host_grads,slices,packed", [(False, 1, True), (True, 1, False),
+                                                      (False, 4, True)],
+                         ids=["device-grads", "host-grads-per-tensor", "sliced"])
+def test_q8_streamed_device_accumulators(K, host_grads, slices, packed):
+    """8-bit accumulators (codes and scales) kept in HBM while the other states
+    stream: every field bit for bit against the oracle."""
+    cfg = small_config(SIZES, K=K, steps=3, units=UNITS)
+    sr = StreamedRunnerQ8(cfg, DeviceGrads(cfg, pin_host=host_grads), n_slots=2,
+                          packed=packed, acc_on_device=True)
+    assert all(t["acc_q"].is_cuda and t["acc_scale"].is_cuda for t in sr.state.tensors)
+    sr.pool.slices(slices, 8192)
+    try:
+        for t in range(cfg.steps):
+            sr.step(t)
+        sr.pool.sync(600_000)
+        compare(sr.state, run_config_q8(cfg, fused=True), f"q8 device acc K={K}")
+    finally:
+        sr.close()
+
+
+def test_q8_streamed_mixed_accumulator_residency_rejected():
+    """Codes on the device with scales in pinned RAM (one tensor) is a mixed unit:
+    rejected before anything is enqueued."""
+    cfg = small_config(SIZES, K=2, steps=1, units=UNITS)
+    sr = StreamedRunnerQ8(cfg, DeviceGrads(cfg), n_slots=2)
+    try:
+        j = cfg.unit_tensors(0)[0]
+        sr.state.tensors[j]["acc_q"] = torch.zeros_like(sr.state.tensors[j]["acc_q"],
+                                                        device="cuda")
+        layers = LayersQ8(sr.state, [cfg.unit_tensors(u) for u in range(cfg.n_units)],
+                          packed=False)
+        arr, keep = layers.build([sr.grads(i, 0, 0) for i in range(len(SIZES))])
+        with pytest.raises(lema.LemaError) as e:
+            lema.lema_stream_layers_q8(sr.pool.handle, arr, 1, sr.hp, 1)
+        assert e.value.status == lema.LEMA_ERR_ARG and "must all be pinned host" in e.value.message
+    finally:
+        sr.close()
+
+
 def test_q8_streamed_host_grads_three_slots_matches_resident():
     cfg = small_config(SIZES, K=3, steps=3, units=UNITS)
     sr = run_streamed(cfg, host_grads=True, n_slots=3)
