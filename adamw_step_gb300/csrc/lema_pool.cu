@@ -131,6 +131,7 @@ struct lema_pool {
     GaveUpFlag gave_up;   // set by an 8-bit step kernel of this pool whose wait ran out
     bool copies_only = false;   // measurement mode: no kernels (lema_pool_copies_only)
     int32_t max_slices = 1;                   // lema_pool_slices (default: whole units)
+    bool slice_first_only = false;            // lema_pool_slice_first_unit
     int64_t min_slice = int64_t(8) << 20;     // elements
     std::mutex mu;
     // Stage tracing (off unless lema_pool_trace enabled it): a timed event pair per
@@ -206,10 +207,13 @@ int new_event(cudaEvent_t* e) {
 
 // The slices of a unit whose packed span holds n_span elements: S pieces, bound[0]
 // = 0 < bound[1] < ... < bound[S] = n_span, inner boundaries on whole chunks, each
-// piece at least the pool's minimum slice; S = 1 for a unit that is not packed.
-int unit_slices(const lema_pool* p, bool packed, int64_t n_span, int64_t* bound) {
+// piece at least the pool's minimum slice; S = 1 for a unit that is not packed, and
+// for every unit but the call's first (slot-using) one when the pool slices only that.
+int unit_slices(const lema_pool* p, bool packed, bool first_unit, int64_t n_span,
+                int64_t* bound) {
     bound[0] = 0;
-    int64_t want = packed ? std::min<int64_t>(p->max_slices, n_span / p->min_slice) : 1;
+    const bool sliced = packed && (first_unit || !p->slice_first_only);
+    int64_t want = sliced ? std::min<int64_t>(p->max_slices, n_span / p->min_slice) : 1;
     want = std::max<int64_t>(1, std::min<int64_t>(want, kMaxSlices));
     int S = 0;
     for (int64_t q = 1; q < want; ++q) {
@@ -480,6 +484,14 @@ extern "C" int lema_pool_slices(lema_pool* pool, int32_t max_slices, int64_t min
     return LEMA_OK;
 }
 
+extern "C" int lema_pool_slice_first_unit(lema_pool* pool, int32_t on) {
+    clear_error();
+    if (!pool) return set_error(LEMA_ERR_ARG, "pool is NULL");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    pool->slice_first_only = on != 0;
+    return LEMA_OK;
+}
+
 extern "C" int lema_pool_copies_only(lema_pool* pool, int32_t on) {
     clear_error();
     if (!pool) return set_error(LEMA_ERR_ARG, "pool is NULL");
@@ -568,6 +580,7 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
     std::vector<AccDesc> ad;
     std::vector<StepDesc> sd;
     std::vector<size_t> waits;
+    int32_t slot_units = 0;   // units of this call that went through a slot so far
     for (int32_t L = 0; L < n_layers; ++L) {
         const lema_layer& ly = layers[L];
         // Accumulators in device memory stay there: read and written in place by the
@@ -599,6 +612,7 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
         }
         Slot& sl = pool->slots[size_t(pool->next_slot % pool->n_slots)];
         pool->next_slot++;
+        const bool first_unit = slot_units++ == 0;
         off.assign(size_t(ly.count), 0);
         for (int32_t j = 1; j < ly.count; ++j)
             off[size_t(j)] = off[size_t(j - 1)] + round_up(ly.tensors[j - 1].n, kTensorAlign);
@@ -614,7 +628,7 @@ int lema::stream_units_locked(lema_pool* pool, const lema_layer* layers, int32_t
         const int64_t base = first < 0 ? 0 : off[size_t(first)];
         const int64_t n_span = first < 0 ? 0 : off[size_t(last)] + ly.tensors[last].n - base;
         int64_t bound[kMaxSlices + 1];
-        const int S = unit_slices(pool, packed, n_span, bound);
+        const int S = unit_slices(pool, packed, first_unit, n_span, bound);
         // The part of tensor j in slice q, as [lo, hi) within the tensor (all of it
         // when the unit is not sliced).
         auto part = [&](int32_t j, int q, int64_t* lo, int64_t* hi) {
@@ -1096,6 +1110,7 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
     std::vector<AccDescQ8> ad;
     std::vector<StepDescQ8> sd;
     std::vector<size_t> waits;
+    int32_t slot_units = 0;
     const auto H2D = cudaMemcpyHostToDevice;
     const auto D2H = cudaMemcpyDeviceToHost;
     auto blocks = [](int64_t n) { return (n + kQBlock - 1) / kQBlock; };
@@ -1129,6 +1144,7 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
         }
         Slot& sl0 = pool->slots[size_t(pool->next_slot % pool->n_slots)];
         pool->next_slot++;
+        const bool first_unit = slot_units++ == 0;
         const SlotQ8 sl = carve_q8(sl0, pool->slot_params);
         off.assign(size_t(ly.count), 0);
         for (int32_t j = 1; j < ly.count; ++j)
@@ -1146,7 +1162,7 @@ int lema::stream_units_q8_locked(lema_pool* pool, const lema_layer_q8* layers, i
         const int64_t base = first < 0 ? 0 : off[size_t(first)];
         const int64_t n_span = first < 0 ? 0 : off[size_t(last)] + ly.tensors[last].n - base;
         int64_t bound[kMaxSlices + 1];
-        const int S = unit_slices(pool, packed, n_span, bound);
+        const int S = unit_slices(pool, packed, first_unit, n_span, bound);
         auto part = [&](int32_t j, int q, int64_t* lo, int64_t* hi) {
             const int64_t n = ly.tensors[j].n, o = off[size_t(j)] - base;
             if (S == 1) { *lo = 0; *hi = n; return; }

@@ -156,6 +156,7 @@ def raw():
     lib.lema_pool_trace.argtypes = [c_void_p, c_int32]
     lib.lema_pool_copies_only.argtypes = [c_void_p, c_int32]
     lib.lema_pool_slices.argtypes = [c_void_p, c_int32, c_int64]
+    lib.lema_pool_slice_first_unit.argtypes = [c_void_p, c_int32]
     lib.lema_pool_trace_read.argtypes = [c_void_p, ctypes.POINTER(LemaTraceEvent), c_int32,
                                          ctypes.POINTER(c_int32)]
     lib.lema_test_fail_copy.argtypes = [c_int64]
@@ -171,7 +172,8 @@ def raw():
                  "lema_stream_layers_disk_q8", "lema_disk_probe", "lema_kernel_wait_timeouts",
                  "lema_pool_sync", "lema_pool_wait_stream", "lema_pool_destroy",
                  "lema_pool_trace", "lema_pool_trace_read", "lema_test_kernel_wait_limit",
-                 "lema_pool_copies_only", "lema_pool_slices", "lema_test_divide_by_constant"):
+                 "lema_pool_copies_only", "lema_pool_slices", "lema_pool_slice_first_unit",
+                 "lema_test_divide_by_constant"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -284,6 +286,11 @@ def lema_pool_slices(pool, max_slices: int, min_slice_params: int) -> None:
     """Split packed units into at most max_slices slices of whole chunks, each at
     least min_slice_params elements, so their copies and kernels overlap."""
     _check(raw().lema_pool_slices(pool, int(max_slices), int(min_slice_params)))
+
+
+def lema_pool_slice_first_unit(pool, on: bool) -> None:
+    """Slice only the first slot-using unit of each streamed call."""
+    _check(raw().lema_pool_slice_first_unit(pool, 1 if on else 0))
 
 
 def lema_pool_copies_only(pool, on: bool) -> None:

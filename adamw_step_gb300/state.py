@@ -185,8 +185,9 @@ class Pool:
     def sync(self, timeout_ms: int = 600_000):
         lema.lema_pool_sync(self.handle, timeout_ms)
 
-    def slices(self, max_slices: int, min_slice_params: int):
+    def slices(self, max_slices: int, min_slice_params: int, first_unit_only=False):
         lema.lema_pool_slices(self.handle, max_slices, min_slice_params)
+        lema.lema_pool_slice_first_unit(self.handle, first_unit_only)
 
     def wait_stream(self, stream=None):
         lema.lema_pool_wait_stream(self.handle, stream)

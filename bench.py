@@ -84,6 +84,9 @@ def parse():
     p.add_argument("--slices", type=int, default=0,
                    help="streamed legs: split each packed unit into at most this many slices "
                         "(lema_pool_slices; 0: the pool's default, whole units)")
+    p.add_argument("--slice-first", action="store_true",
+                   help="streamed legs with --slices: slice only the first unit of each call "
+                        "(lema_pool_slice_first_unit)")
     p.add_argument("--slots", type=int, default=0,
                    help="streamed legs: VRAM slots of the pool (0: the workload's own, 2)")
     p.add_argument("--min-slice", type=int, default=8 << 20,
@@ -406,7 +409,7 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
                                                       n_slots=getattr(args, "slots", 0) or None,
                                                       acc_on_device=acc_dev)
     if getattr(args, "slices", 0):
-        sr.pool.slices(args.slices, args.min_slice)
+        sr.pool.slices(args.slices, args.min_slice, getattr(args, "slice_first", False))
     huge = anon_huge_bytes()
     for t in range(warmup):
         sr.step(t, stream)
@@ -451,7 +454,8 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
            "host_state_bytes": sr.state.pinned.nbytes, "anon_huge_page_bytes": huge,
            "compute_hidden": hidden,
            "slices": {"max": getattr(args, "slices", 0) or "pool default (1: whole units)",
-                      "min_params": getattr(args, "min_slice", 8 << 20)},
+                      "min_params": getattr(args, "min_slice", 8 << 20),
+                      "first_unit_only": getattr(args, "slice_first", False)},
            "path": f"lema_stream_layers{'_q8' if q8 else ''}, "
                    f"{getattr(args, 'slots', 0) or cfg.n_slots} VRAM slots, "
                    f"3 streams, {'8-bit' if q8 else 'fp32'} states "

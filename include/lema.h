@@ -539,6 +539,14 @@ int lema_pool_destroy(lema_pool* pool);
  * raised).  Applies to calls made after it.  Returns LEMA_OK or LEMA_ERR_ARG. */
 int lema_pool_slices(lema_pool* pool, int32_t max_slices, int64_t min_slice_params);
 
+/* With `on` != 0, lema_pool_slices applies only to the first unit of each streamed
+ * call that goes through a slot; the other units move whole.  The first unit is the
+ * one whose load no earlier copy of the call hides (the results of a call cannot go
+ * back before it has arrived and been computed), while slicing the others makes the
+ * two copy directions overlap more.  Off (0) by default.  Applies to calls made
+ * after it.  Returns LEMA_OK or LEMA_ERR_ARG (pool is NULL). */
+int lema_pool_slice_first_unit(lema_pool* pool, int32_t on);
+
 /* Measurement mode of a pool: with `on` != 0, every later streamed call
  * (lema_stream_layers, lema_stream_layers_q8 and their disk forms) enqueues its
  * copies, events and stream ordering exactly as usual but launches no kernel, so

@@ -100,6 +100,7 @@ def test_pool_validation_before_cuda(lib):
     assert lib.lema_stream_layers_q8(None, Q, 1, 1, ctypes.byref(hp), 1, None) == -1
     assert lib.lema_pool_destroy(None) == 0
     assert lib.lema_pool_slices(None, 4, 8192) == -1
+    assert lib.lema_pool_slice_first_unit(None, 1) == -1
     assert lib.lema_pool_copies_only(None, 1) == -1
     # the division check takes divisors in (2^-27, 1] only (rejected before any CUDA call)
     d = (ctypes.c_float * 1)(2.0)

@@ -4,8 +4,8 @@ Each case draws a tensor count (on both sides of the by-value descriptor table's
 64-tensor limit), ragged sizes (empty tensors included), K, the number of steps,
 the hyperparameters (betas, lr, eps, weight decay inside the method's domain) and
 the form (fused: last grad folded in; unfused: K accumulates, then the step), and
-runs it resident and streamed (through a pool of two or three slots), with fp32
-states and with 8-bit states.  Every field must equal the oracle's bits.  The seeds
+runs it resident and streamed (through a pool of two or three slots; every third
+case with its accumulators kept in HBM), with fp32 states and with 8-bit states.  Every field must equal the oracle's bits.  The seeds
 are fixed, so every run checks the same cases.
 """
 from __future__ import annotations
@@ -93,7 +93,8 @@ def test_fuzz_resident_q8(seed):
 @pytest.mark.parametrize("seed", range(CASES))
 def test_fuzz_streamed_fp32(seed):
     cfg, _, n_slots = draw(seed)
-    sr = StreamedRunner(cfg, DeviceGrads(cfg), n_slots=n_slots)
+    # every third case keeps its accumulators in HBM (only the states stream)
+    sr = StreamedRunner(cfg, DeviceGrads(cfg), n_slots=n_slots, acc_on_device=seed % 3 == 1)
     try:
         for t in range(cfg.steps):
             sr.step(t)
@@ -111,7 +112,7 @@ def test_fuzz_streamed_fp32(seed):
 @pytest.mark.parametrize("seed", range(CASES))
 def test_fuzz_streamed_q8(seed):
     cfg, _, n_slots = draw(seed)
-    sr = StreamedRunnerQ8(cfg, DeviceGrads(cfg), n_slots=n_slots)
+    sr = StreamedRunnerQ8(cfg, DeviceGrads(cfg), n_slots=n_slots, acc_on_device=seed % 3 == 1)
     try:
         for t in range(cfg.steps):
             sr.step(t)

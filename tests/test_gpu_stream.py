@@ -66,13 +66,15 @@ def test_streamed_small_matches_oracle(host_grads, n_slots, packed):
     sr.close()
 
 
+@pytest.mark.parametrize("first_only", [False, True], ids=["every-unit", "first-unit"])
 @pytest.mark.parametrize("host_grads", [False, True], ids=["device-grads", "host-grads"])
-def test_streamed_sliced_units_match_oracle(host_grads):
+def test_streamed_sliced_units_match_oracle(host_grads, first_only):
     """Packed units split into up to 4 slices of whole chunks (slice boundaries
-    inside tensors and between them): same bits as the oracle."""
+    inside tensors and between them; every unit, or only each call's first): same
+    bits as the oracle."""
     cfg = small_config(RAGGED, K=3, steps=3, units=ragged_units())
     sr = StreamedRunner(cfg, DeviceGrads(cfg, pin_host=host_grads), n_slots=2, packed=True)
-    sr.pool.slices(4, 8192)
+    sr.pool.slices(4, 8192, first_unit_only=first_only)
     for t in range(cfg.steps):
         sr.step(t)
     sr.pool.sync(600_000)
@@ -82,9 +84,10 @@ def test_streamed_sliced_units_match_oracle(host_grads):
 
 @pytest.mark.parametrize("K", [1, 2, 3])
 @pytest.mark.parametrize("host_grads,slices,packed", [(False, 1, True), (True, 1, False),
-                                                      (False, 4, True), (True, 4, True)],
+                                                      (False, 4, True), (True, 4, True),
+                                                      (False, 2, True)],
                          ids=["device-grads", "host-grads-per-tensor", "sliced",
-                              "host-grads-sliced"])
+                              "host-grads-sliced", "first-unit-sliced"])
 def test_streamed_device_accumulators_match_oracle(K, host_grads, slices, packed):
     """Accumulators kept in HBM while the optimizer states stream: the same bits as
     the oracle, the device acc holding micro-steps 1..K-1 of the last step (as the
@@ -93,7 +96,7 @@ def test_streamed_device_accumulators_match_oracle(K, host_grads, slices, packed
     sr = StreamedRunner(cfg, DeviceGrads(cfg, pin_host=host_grads), n_slots=2, packed=packed,
                         acc_on_device=True)
     assert all(t["acc"].is_cuda for t in sr.state.tensors)
-    sr.pool.slices(slices, 8192)
+    sr.pool.slices(slices, 8192, first_unit_only=slices == 2)
     try:
         for t in range(cfg.steps):
             sr.step(t)

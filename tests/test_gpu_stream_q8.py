@@ -50,13 +50,14 @@ def compare(state, ref, label, tensors=None):
                 f"{label} tensor {j} {f}: first mismatch at byte {np.flatnonzero(~same)[:3]}"
 
 
+@pytest.mark.parametrize("first_only", [False, True], ids=["every-unit", "first-unit"])
 @pytest.mark.parametrize("host_grads", [False, True], ids=["device-grads", "host-grads"])
-def test_q8_streamed_sliced_units(host_grads):
-    """Packed 8-bit units split into up to 4 slices of whole chunks: every field
-    bit for bit against the oracle."""
+def test_q8_streamed_sliced_units(host_grads, first_only):
+    """Packed 8-bit units split into up to 4 slices of whole chunks (every unit, or
+    only each call's first): every field bit for bit against the oracle."""
     cfg = small_config(SIZES, K=3, steps=2, units=UNITS)
     sr = StreamedRunnerQ8(cfg, DeviceGrads(cfg, pin_host=host_grads), n_slots=2, packed=True)
-    sr.pool.slices(4, 8192)
+    sr.pool.slices(4, 8192, first_unit_only=first_only)
     try:
         for t in range(cfg.steps):
             sr.step(t)
