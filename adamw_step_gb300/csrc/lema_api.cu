@@ -451,33 +451,38 @@ int launch_by_value(const Desc* descs, int32_t count, cudaStream_t stream, int v
 
 }  // namespace
 
-int run_accum(const AccDesc* descs, int32_t count, cudaStream_t stream) {
+int run_accum(const AccDesc* descs, int32_t count, cudaStream_t stream, bool pdl) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (count <= kValueTableMax)
         return launch_by_value(
             descs, count, stream, validate_accum(descs, count),
             [&](const AccDesc* d, const Chunk* c, int64_t n) {
-                return launch_accum_v(d, count, c, n, stream);
+                return launch_accum_v(d, count, c, n, stream, pdl);
             },
             "accum_grad launch");
     return stage_and_launch(
         descs, count, stream, validate_accum(descs, count),
-        [&](const AccDesc* d, const Chunk* c, int64_t n) { return launch_accum(d, c, n, stream); },
+        [&](const AccDesc* d, const Chunk* c, int64_t n) {
+            return launch_accum(d, c, n, stream, pdl);
+        },
         "accum_grad launch");
 }
 
-int run_step(const StepDesc* descs, int32_t count, const StepScalars& s, cudaStream_t stream) {
+int run_step(const StepDesc* descs, int32_t count, const StepScalars& s, cudaStream_t stream,
+             bool pdl) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (count <= kValueTableMax)
         return launch_by_value(
             descs, count, stream, validate_step(descs, count),
             [&](const StepDesc* d, const Chunk* c, int64_t n) {
-                return launch_step_v(d, count, c, n, s, stream);
+                return launch_step_v(d, count, c, n, s, stream, pdl);
             },
             "adamw step launch");
     return stage_and_launch(
         descs, count, stream, validate_step(descs, count),
-        [&](const StepDesc* d, const Chunk* c, int64_t n) { return launch_step(d, c, n, s, stream); },
+        [&](const StepDesc* d, const Chunk* c, int64_t n) {
+            return launch_step(d, c, n, s, stream, pdl);
+        },
         "adamw step launch");
 }
 
@@ -668,7 +673,7 @@ extern "C" int lema_accum_grad(const lema_grad* grads, int32_t count, void* cuda
         const bool first = (g.flags & LEMA_GRAD_FIRST) != 0;
         d[j] = AccDesc{first ? nullptr : g.acc, g.acc, g.grad_bf16, g.n};
     }
-    return run_accum(d.data(), count, static_cast<cudaStream_t>(cuda_stream));
+    return run_accum(d.data(), count, static_cast<cudaStream_t>(cuda_stream), true);
 }
 
 extern "C" int lema_adamw_step(const lema_tensor* tensors, int32_t count, int64_t step, double lr,
@@ -722,7 +727,7 @@ extern "C" int lema_adamw_step(const lema_tensor* tensors, int32_t count, int64_
             if (p && !aligned16(p))
                 return set_error(LEMA_ERR_ALIGN, "tensor %d: base address not 16-byte aligned", j);
     }
-    return run_step(d.data(), count, s, static_cast<cudaStream_t>(cuda_stream));
+    return run_step(d.data(), count, s, static_cast<cudaStream_t>(cuda_stream), true);
 }
 
 extern "C" int lema_accum_grad_q8(const lema_grad_q8* grads, int32_t count, void* cuda_stream) {

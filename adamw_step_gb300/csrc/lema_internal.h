@@ -85,10 +85,12 @@ struct StepScalars {
 
 // Kernel launchers (lema_kernels.cu; the 8-bit ones are declared in lema_q8.h).
 // `descs` and `chunks` are device tables.
+// pdl: launch with programmatic stream serialization (the kernel is scheduled while
+// the one before it on the stream drains, and waits for it before any memory access).
 cudaError_t launch_accum(const AccDesc* descs, const Chunk* chunks, int64_t n_chunks,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool pdl = false);
 cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks, int64_t n_chunks,
-                        const StepScalars& s, cudaStream_t stream);
+                        const StepScalars& s, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_merge(const MergeDesc* descs, const Chunk* chunks, int64_t n_chunks,
                          cudaStream_t stream);
 // A descriptor table of up to N tensors passed by value as a kernel parameter
@@ -104,9 +106,10 @@ struct DescTable {
 constexpr int kValueTableSmall = 16;   // 16 x 112 B = 1.8 KB of parameters
 constexpr int kValueTableMax = 64;     // 64 x 112 B = 7.2 KB
 cudaError_t launch_accum_v(const AccDesc* host_descs, int32_t count, const Chunk* chunks,
-                           int64_t n_chunks, cudaStream_t stream);
+                           int64_t n_chunks, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_step_v(const StepDesc* host_descs, int32_t count, const Chunk* chunks,
-                          int64_t n_chunks, const StepScalars& s, cudaStream_t stream);
+                          int64_t n_chunks, const StepScalars& s, cudaStream_t stream,
+                          bool pdl = false);
 // SM-driven copy of `bytes` (a multiple of 16) from pinned host to device memory.
 cudaError_t launch_install(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 
@@ -119,8 +122,10 @@ int make_scalars(int64_t step, double lr, double beta1, double beta2, double eps
 // The fp32 reciprocal of a positive normal c, correctly rounded (RN(1/c)).
 float rcp_rn(float c);
 // Validate + build-or-reuse the device table + launch.  Host arrays of descriptors.
-int run_accum(const AccDesc* descs, int32_t count, cudaStream_t stream);
-int run_step(const StepDesc* descs, int32_t count, const StepScalars& s, cudaStream_t stream);
+// pdl: as the launchers' (the public resident entry points pass true).
+int run_accum(const AccDesc* descs, int32_t count, cudaStream_t stream, bool pdl = false);
+int run_step(const StepDesc* descs, int32_t count, const StepScalars& s, cudaStream_t stream,
+             bool pdl = false);
 int run_merge(const MergeDesc* descs, int32_t count, cudaStream_t stream);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

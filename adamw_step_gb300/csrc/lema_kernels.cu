@@ -150,10 +150,23 @@ __device__ __forceinline__ void adamw_chunk(const StepDesc* __restrict__ dp, con
     }
 }
 
+// Programmatic dependent launch.  The accumulate and step kernels may be launched
+// with programmatic stream serialization, so that their CTAs are scheduled while
+// the kernel before them on the stream drains (the launch latency of a small
+// launch then overlaps that kernel's tail).  Each CTA first waits for the kernels
+// it depends on to complete and their memory to be visible, before any global
+// access, and then lets the next launch be scheduled.  Launched the plain way,
+// both instructions return at once.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <bool kPow2, int kSplit>
 __global__ void __launch_bounds__(kThreads)
 adamw_fused_kernel(const StepDesc* __restrict__ descs, const Chunk* __restrict__ chunks,
                    const StepScalars s) {
+    pdl_enter();
     const Chunk c = chunks[blockIdx.x / kSplit];
     adamw_chunk<kPow2, kSplit>(descs + c.tensor, c, s);
 }
@@ -162,6 +175,7 @@ template <bool kPow2, int kSplit, int N>
 __global__ void __launch_bounds__(kThreads)
 adamw_fused_kernel_v(const __grid_constant__ DescTable<StepDesc, N> t,
                      const Chunk* __restrict__ chunks, const StepScalars s) {
+    pdl_enter();
     const Chunk c = chunks[blockIdx.x / kSplit];
     adamw_chunk<kPow2, kSplit>(&t.d[c.tensor], c, s);
 }
@@ -201,6 +215,7 @@ __device__ __forceinline__ void accum_chunk(const AccDesc* __restrict__ dp, cons
 template <int kSplit>
 __global__ void __launch_bounds__(kThreads)
 accum_grad_kernel(const AccDesc* __restrict__ descs, const Chunk* __restrict__ chunks) {
+    pdl_enter();
     const Chunk c = chunks[blockIdx.x / kSplit];
     accum_chunk<kSplit>(descs + c.tensor, c);
 }
@@ -209,6 +224,7 @@ template <int kSplit, int N>
 __global__ void __launch_bounds__(kThreads)
 accum_grad_kernel_v(const __grid_constant__ DescTable<AccDesc, N> t,
                     const Chunk* __restrict__ chunks) {
+    pdl_enter();
     const Chunk c = chunks[blockIdx.x / kSplit];
     accum_chunk<kSplit>(&t.d[c.tensor], c);
 }
@@ -293,17 +309,38 @@ cudaError_t split_launch(int64_t n_chunks, bool* split) {
     return cudaSuccess;
 }
 
+namespace {
+
+// One launch of kThreads-thread CTAs, with programmatic stream serialization when
+// `pdl` (see pdl_enter).
+template <typename... P, typename... A>
+cudaError_t launch_k(void (*kernel)(P...), unsigned grid, cudaStream_t stream, bool pdl,
+                     A... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
+
 cudaError_t launch_accum(const AccDesc* descs, const Chunk* chunks, int64_t n_chunks,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool pdl) {
     if (n_chunks <= 0) return cudaSuccess;
     bool split = false;
     const cudaError_t e = split_launch(n_chunks, &split);
     if (e != cudaSuccess) return e;
     if (split)
-        accum_grad_kernel<kIters><<<dim3(unsigned(n_chunks * kIters)), kThreads, 0, stream>>>(descs, chunks);
-    else
-        accum_grad_kernel<1><<<dim3(unsigned(n_chunks)), kThreads, 0, stream>>>(descs, chunks);
-    return cudaGetLastError();
+        return launch_k(accum_grad_kernel<kIters>, unsigned(n_chunks * kIters), stream, pdl,
+                        descs, chunks);
+    return launch_k(accum_grad_kernel<1>, unsigned(n_chunks), stream, pdl, descs, chunks);
 }
 
 namespace {
@@ -317,53 +354,52 @@ DescTable<D, N> table_of(const D* host, int32_t count) {
 }
 
 template <int N>
-void accum_v(const AccDesc* host, int32_t count, const Chunk* chunks, int64_t n_chunks, bool split,
-             cudaStream_t stream) {
+cudaError_t accum_v(const AccDesc* host, int32_t count, const Chunk* chunks, int64_t n_chunks,
+                    bool split, cudaStream_t stream, bool pdl) {
     const DescTable<AccDesc, N> t = table_of<AccDesc, N>(host, count);
     if (split)
-        accum_grad_kernel_v<kIters, N><<<dim3(unsigned(n_chunks * kIters)), kThreads, 0, stream>>>(t, chunks);
-    else
-        accum_grad_kernel_v<1, N><<<dim3(unsigned(n_chunks)), kThreads, 0, stream>>>(t, chunks);
+        return launch_k(accum_grad_kernel_v<kIters, N>, unsigned(n_chunks * kIters), stream, pdl,
+                        t, chunks);
+    return launch_k(accum_grad_kernel_v<1, N>, unsigned(n_chunks), stream, pdl, t, chunks);
 }
 
 template <int N>
-void step_v(const StepDesc* host, int32_t count, const Chunk* chunks, int64_t n_chunks, bool split,
-            const StepScalars& s, cudaStream_t stream) {
+cudaError_t step_v(const StepDesc* host, int32_t count, const Chunk* chunks, int64_t n_chunks,
+                   bool split, const StepScalars& s, cudaStream_t stream, bool pdl) {
     const DescTable<StepDesc, N> t = table_of<StepDesc, N>(host, count);
-    const dim3 whole(static_cast<unsigned>(n_chunks)), parts(static_cast<unsigned>(n_chunks * kIters));
+    const unsigned whole = unsigned(n_chunks), parts = unsigned(n_chunks * kIters);
     if (s.accum_pow2) {
-        if (split) adamw_fused_kernel_v<true, kIters, N><<<parts, kThreads, 0, stream>>>(t, chunks, s);
-        else adamw_fused_kernel_v<true, 1, N><<<whole, kThreads, 0, stream>>>(t, chunks, s);
-    } else {
-        if (split) adamw_fused_kernel_v<false, kIters, N><<<parts, kThreads, 0, stream>>>(t, chunks, s);
-        else adamw_fused_kernel_v<false, 1, N><<<whole, kThreads, 0, stream>>>(t, chunks, s);
+        if (split) return launch_k(adamw_fused_kernel_v<true, kIters, N>, parts, stream, pdl, t, chunks, s);
+        return launch_k(adamw_fused_kernel_v<true, 1, N>, whole, stream, pdl, t, chunks, s);
     }
+    if (split) return launch_k(adamw_fused_kernel_v<false, kIters, N>, parts, stream, pdl, t, chunks, s);
+    return launch_k(adamw_fused_kernel_v<false, 1, N>, whole, stream, pdl, t, chunks, s);
 }
 
 }  // namespace
 
 cudaError_t launch_accum_v(const AccDesc* host_descs, int32_t count, const Chunk* chunks,
-                           int64_t n_chunks, cudaStream_t stream) {
+                           int64_t n_chunks, cudaStream_t stream, bool pdl) {
     if (n_chunks <= 0) return cudaSuccess;
     if (count > kValueTableMax) return cudaErrorInvalidValue;
     bool split = false;
     const cudaError_t e = split_launch(n_chunks, &split);
     if (e != cudaSuccess) return e;
-    if (count <= kValueTableSmall) accum_v<kValueTableSmall>(host_descs, count, chunks, n_chunks, split, stream);
-    else accum_v<kValueTableMax>(host_descs, count, chunks, n_chunks, split, stream);
-    return cudaGetLastError();
+    if (count <= kValueTableSmall)
+        return accum_v<kValueTableSmall>(host_descs, count, chunks, n_chunks, split, stream, pdl);
+    return accum_v<kValueTableMax>(host_descs, count, chunks, n_chunks, split, stream, pdl);
 }
 
 cudaError_t launch_step_v(const StepDesc* host_descs, int32_t count, const Chunk* chunks,
-                          int64_t n_chunks, const StepScalars& s, cudaStream_t stream) {
+                          int64_t n_chunks, const StepScalars& s, cudaStream_t stream, bool pdl) {
     if (n_chunks <= 0) return cudaSuccess;
     if (count > kValueTableMax) return cudaErrorInvalidValue;
     bool split = false;
     const cudaError_t e = split_launch(n_chunks, &split);
     if (e != cudaSuccess) return e;
-    if (count <= kValueTableSmall) step_v<kValueTableSmall>(host_descs, count, chunks, n_chunks, split, s, stream);
-    else step_v<kValueTableMax>(host_descs, count, chunks, n_chunks, split, s, stream);
-    return cudaGetLastError();
+    if (count <= kValueTableSmall)
+        return step_v<kValueTableSmall>(host_descs, count, chunks, n_chunks, split, s, stream, pdl);
+    return step_v<kValueTableMax>(host_descs, count, chunks, n_chunks, split, s, stream, pdl);
 }
 
 cudaError_t launch_merge(const MergeDesc* descs, const Chunk* chunks, int64_t n_chunks,
@@ -375,20 +411,18 @@ cudaError_t launch_merge(const MergeDesc* descs, const Chunk* chunks, int64_t n_
 
 
 cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks, int64_t n_chunks,
-                        const StepScalars& s, cudaStream_t stream) {
+                        const StepScalars& s, cudaStream_t stream, bool pdl) {
     if (n_chunks <= 0) return cudaSuccess;
     bool split = false;
     const cudaError_t e = split_launch(n_chunks, &split);
     if (e != cudaSuccess) return e;
-    const dim3 whole(static_cast<unsigned>(n_chunks)), parts(static_cast<unsigned>(n_chunks * kIters));
+    const unsigned whole = unsigned(n_chunks), parts = unsigned(n_chunks * kIters);
     if (s.accum_pow2) {
-        if (split) adamw_fused_kernel<true, kIters><<<parts, kThreads, 0, stream>>>(descs, chunks, s);
-        else adamw_fused_kernel<true, 1><<<whole, kThreads, 0, stream>>>(descs, chunks, s);
-    } else {
-        if (split) adamw_fused_kernel<false, kIters><<<parts, kThreads, 0, stream>>>(descs, chunks, s);
-        else adamw_fused_kernel<false, 1><<<whole, kThreads, 0, stream>>>(descs, chunks, s);
+        if (split) return launch_k(adamw_fused_kernel<true, kIters>, parts, stream, pdl, descs, chunks, s);
+        return launch_k(adamw_fused_kernel<true, 1>, whole, stream, pdl, descs, chunks, s);
     }
-    return cudaGetLastError();
+    if (split) return launch_k(adamw_fused_kernel<false, kIters>, parts, stream, pdl, descs, chunks, s);
+    return launch_k(adamw_fused_kernel<false, 1>, whole, stream, pdl, descs, chunks, s);
 }
 
 }  // namespace lema

@@ -27,6 +27,11 @@
  *     the slot memory, streams and events.
  *   - Streams: `cuda_stream` is a cudaStream_t (NULL = the legacy default stream).
  *     Calls enqueue work and return; they do not synchronize the host.
+ *     lema_accum_grad and lema_adamw_step launch their kernels with programmatic
+ *     dependent launch: the kernel's blocks may be scheduled while the kernel
+ *     before it on the stream finishes, and wait for it to complete (its memory
+ *     visible) before they touch any buffer, so stream order holds as for a plain
+ *     launch; back-to-back small calls lose less time between kernels.
  *   - Errors: every call returns a lema_status.  Arguments are validated before
  *     anything is enqueued; on a validation failure nothing is launched or copied.
  *     lema_last_error() gives a message for the calling thread's last failure.
