@@ -94,7 +94,8 @@ int record(cudaEvent_t ev, cudaStream_t s) {
     return e == cudaSuccess ? LEMA_OK : cuda_error(e, "cudaEventRecord");
 }
 
-// 0 = not pinned/accessible host memory, 1 = pinned host, 2 = device (or managed).
+// 1 = pinned host, 2 = memory of the current device (or managed), 0 = anything else
+// (pageable host memory, another GPU's memory).
 int memory_kind(const void* p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -102,7 +103,15 @@ int memory_kind(const void* p) {
         return 0;
     }
     if (a.type == cudaMemoryTypeHost) return 1;
-    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return 2;
+    if (a.type == cudaMemoryTypeManaged) return 2;
+    if (a.type == cudaMemoryTypeDevice) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return a.device == dev ? 2 : 0;
+    }
     return 0;
 }
 
@@ -265,8 +274,8 @@ int check_acc_kind(const void* const* bufs, int n_bufs, int32_t L, int32_t j,
         const int k = cached_kind(kinds, p);
         if (k == 0)
             return set_error(LEMA_ERR_ARG,
-                             "unit %d tensor %d: accumulator must be pinned host or device memory",
-                             L, j);
+                             "unit %d tensor %d: accumulator must be pinned host memory or memory "
+                             "of the pool's GPU", L, j);
         if (*kind != 0 && k != *kind)
             return set_error(LEMA_ERR_ARG,
                              "unit %d tensor %d: a unit's accumulators must all be pinned host "
@@ -317,7 +326,8 @@ int check_streamed_unit(const lema_layer& ly, int32_t L, int32_t k, bool final_s
         const int kind = cached_kind(kinds, g);
         if (kind == 0)
             return set_error(LEMA_ERR_ARG,
-                             "unit %d tensor %d: grad must be device or pinned host memory", L, j);
+                             "unit %d tensor %d: grad must be memory of the pool's GPU or pinned "
+                             "host memory", L, j);
         grad_on_host.back() = (kind == 1);
     }
     (void)k;
@@ -1004,7 +1014,8 @@ int check_streamed_unit_q8(const lema_layer_q8& ly, int32_t L, bool final_step,
         const int kind = cached_kind(kinds, g);
         if (kind == 0)
             return set_error(LEMA_ERR_ARG,
-                             "unit %d tensor %d: grad must be device or pinned host memory", L, j);
+                             "unit %d tensor %d: grad must be memory of the pool's GPU or pinned "
+                             "host memory", L, j);
         grad_on_host.back() = (kind == 1);
     }
     *acc_on_device = acc_kind == 2;

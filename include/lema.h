@@ -299,7 +299,8 @@ typedef struct lema_adamw_hparams {
 /* One streaming unit (a decoder layer, the embedding, the LM head, ...).
  *   tensors  host array of `count` lema_tensor
  *   grads    host array of `count` pointers to this micro-step's bf16 grads, each
- *            either device memory or pinned host memory (then copied to the slot)
+ *            either memory of the pool's device or pinned host memory (then copied
+ *            to the slot)
  *   flags    LEMA_UNIT_PACKED: the unit's host states are laid out like a slot.  For
  *            every state field (master, m, v, acc, delta, orig_bf16, w_bf16, and the
  *            *_out fields when set), tensor j's pointer is the first non-empty
@@ -349,8 +350,8 @@ int lema_pool_create(int32_t n_slots, int64_t slot_params, lema_pool** out);
  * Accumulator residency (page "LEMA: Layer-wise Efficient Memory Abstraction",
  * section "TensorStore: Unified Streaming Core": weights, optimizer states and
  * gradient accumulators each with a residency policy of their own): a unit's acc
- * may instead be device memory (16-byte aligned, all of the unit's non-empty
- * tensors alike; a unit mixing the two is rejected with LEMA_ERR_ARG).  It then
+ * may instead be memory of the pool's device (16-byte aligned, all of the unit's
+ * non-empty tensors alike; a unit mixing the two is rejected with LEMA_ERR_ARG).  It then
  * stays in HBM: the compute stage reads and updates it in place (k < K) or reads it
  * (k == K), and no acc copy crosses the host link, which leaves master, m, v, orig
  * in and master', m', v', delta, w_bf16 out at k == K, and nothing but host grads
