@@ -80,3 +80,31 @@ def test_bench_l2_label_follows_the_bytes_per_launch():
     assert "within the 129 MB L2" in bench.l2_label([6e6, 10e6])
     mixed = bench.l2_label([27e6, 45e6, 173e6])
     assert "partly L2-served" in mixed and "27-173 MB" in mixed
+
+
+def test_bench_traffic_figures_match_the_current_kernels():
+    """The committed DRAM counters are keyed by the kernel families' current code,
+    so the bench line reports them (a stale key would make it report null)."""
+    import bench
+    for kind in ("accum_grad_first", "accum_grad", "adamw_fused", "accum_grad_first_q8",
+                 "accum_grad_q8", "adamw_fused_q8"):
+        t = bench.ncu_traffic(kind)
+        assert t is not None, kind
+        # every byte streamed once per launch: no more than 1 % above the algorithmic
+        # bytes, and at most 5 % below (reads the L2 still held from the launch before)
+        alg = bench.BYTES[kind]
+        assert -0.05 * alg <= t - alg <= 0.01 * alg, (kind, t)
+
+
+def test_bench_streamed_options_parse(monkeypatch):
+    """The streamed legs' options: accumulators in HBM, slicing of every unit or only
+    each call's first."""
+    import sys
+    import bench
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--config", "3", "--acc-on-device",
+                                      "--slices", "2", "--slice-first", "--q8"])
+    a = bench.parse()
+    assert a.config == 3 and a.acc_on_device and a.slices == 2 and a.slice_first and a.q8
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    assert a.config == 2 and not a.acc_on_device and a.slices == 0 and not a.slice_first
