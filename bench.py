@@ -394,6 +394,20 @@ def config_block(cfg, args, world, l2=None):
 
 # ----------------------------------------------------------------- streamed leg
 
+def best_link_peaks(before: dict, after: dict) -> dict:
+    """Per direction, the better of the pinned-copy probes taken before and after a
+    leg's timed steps: the host link is shared with the rest of the machine, and a
+    probe that met a slow moment would understate the link and overstate a fraction
+    of it."""
+    return {k: max(before[k], after[k]) for k in ("h2d_gbs", "d2h_gbs", "bidir_gbs")}
+
+
+def probes_record(before: dict, after: dict) -> dict:
+    keys = ("h2d_gbs", "d2h_gbs", "bidir_gbs")
+    return {"before": {k: round(before[k], 1) for k in keys},
+            "after": {k: round(after[k], 1) for k in keys}}
+
+
 def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
     """Whole optimizer steps through lema_stream_layers (lema_stream_layers_q8 with
     --q8) with the states in pinned host RAM (grads pinned too when host_grads).
@@ -435,6 +449,12 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
     hidden = None if getattr(args, "no_hidden", False) else \
         copies_only_steps(sr, stream, world, steps, warmup, el / steps)
     h2d, d2h = sr.link_bytes_per_step(host_grads=host_grads)
+    host_state_bytes = sr.state.pinned.nbytes
+    sr.close()
+    del sr
+    torch.cuda.empty_cache()
+    probed, reprobed = peaks, host_link_peaks(1 << 30, 3)
+    peaks = best_link_peaks(probed, reprobed)
     floor = link_time_floor(h2d, d2h, peaks)
     per_step = el / steps
     each = sorted(a.elapsed_time(b) for a, b in marks)
@@ -449,9 +469,10 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
            # show the pipeline's own rate when a few steps meet outside traffic
            "ms_per_step_median": median_ms, "link_frac_median": 1e3 * floor / median_ms,
            "link_peaks_gbs": {k: round(peaks[k], 1) for k in ("h2d_gbs", "d2h_gbs", "bidir_gbs")},
+           "link_probes_gbs": probes_record(probed, reprobed),
            # host RAM of this process backed by transparent huge pages once the
            # states were allocated (the rest uses base pages)
-           "host_state_bytes": sr.state.pinned.nbytes, "anon_huge_page_bytes": huge,
+           "host_state_bytes": host_state_bytes, "anon_huge_page_bytes": huge,
            "compute_hidden": hidden,
            "slices": {"max": getattr(args, "slices", 0) or "pool default (1: whole units)",
                       "min_params": getattr(args, "min_slice", 8 << 20),
@@ -461,9 +482,6 @@ def streamed_leg(cfg, args, world, stream, host_grads, steps, warmup=2):
                    f"3 streams, {'8-bit' if q8 else 'fp32'} states "
                    f"{'and bf16 grads ' if host_grads else ''}in pinned host RAM"
                    f"{', accumulators resident in HBM' if acc_dev else ''}"}
-    sr.close()
-    del sr
-    torch.cuda.empty_cache()
     return out
 
 
@@ -552,18 +570,21 @@ def resident_e2e_leg(cfg, args, world, stream, steps, warmup=2):
     barrier(world)
     el = reduce_max(marks[0][0].elapsed_time(marks[-1][1]) / 1e3, world)
     h2d, d2h = r.h2d_bytes_per_step(), r.d2h_bytes_per_step()
-    floor = link_time_floor(h2d, d2h, peaks)
     each = sorted(a.elapsed_time(b) for a, b in marks)
     med = each[len(each) // 2]
     r.close()
     del r
     torch.cuda.empty_cache()
+    probed, reprobed = peaks, host_link_peaks(1 << 30, 3)
+    peaks = best_link_peaks(probed, reprobed)
+    floor = link_time_floor(h2d, d2h, peaks)
     return {"value": world * cfg.params * steps / el, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": 1e3 * el / steps, "ms_per_step_median": med,
             "link_floor_ms": 1e3 * floor, "link_frac": floor / (el / steps),
             "link_frac_median": 1e3 * floor / med,
             "link_peaks_gbs": {k: round(peaks[k], 1) for k in ("h2d_gbs", "d2h_gbs", "bidir_gbs")},
+            "link_probes_gbs": probes_record(probed, reprobed),
             "path": f"{'8-bit' if q8 else 'fp32'} states resident in HBM; each micro-step's "
                     "bf16 grads H2D from pinned host memory (copy stream, double-buffered), "
                     f"lema_accum_grad{'_q8' if q8 else ''} / lema_adamw_step{'_q8' if q8 else ''}, "
