@@ -108,3 +108,20 @@ def test_bench_streamed_options_parse(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py"])
     a = bench.parse()
     assert a.config == 2 and not a.acc_on_device and a.slices == 0 and not a.slice_first
+
+
+def test_link_floor_uses_the_better_probe_per_direction():
+    """A probe that met a slow moment of the shared host must not lower the link
+    peaks the floor divides by."""
+    import bench
+    from adamw_step_gb300.probes import link_time_floor
+    slow = {"h2d_gbs": 88.1, "d2h_gbs": 192.2, "bidir_gbs": 91.1}
+    fast = {"h2d_gbs": 210.0, "d2h_gbs": 190.0, "bidir_gbs": 339.0}
+    best = bench.best_link_peaks(slow, fast)
+    assert best == {"h2d_gbs": 210.0, "d2h_gbs": 192.2, "bidir_gbs": 339.0}
+    assert bench.best_link_peaks(fast, slow) == best
+    h2d, d2h = 28.6e9, 33.0e9
+    assert link_time_floor(h2d, d2h, best) <= min(link_time_floor(h2d, d2h, slow),
+                                                   link_time_floor(h2d, d2h, fast))
+    rec = bench.probes_record(slow, fast)
+    assert rec["before"]["h2d_gbs"] == 88.1 and rec["after"]["h2d_gbs"] == 210.0
